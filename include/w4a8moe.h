@@ -1,0 +1,212 @@
+/*
+ * w4a8moe.h -- C ABI of the GB300 (sm_103a) W4AFP8 mixture-of-experts hot path.
+ *
+ * W4AFP8: int4 weights with fp32 scales per 128 consecutive K, times FP8 E4M3
+ * activations quantised per token per 128 columns, fp32 accumulation, bf16
+ * outputs.  The layer is the workflow of the SGLang PR #7762 page ("support
+ * DeepSeek-R1-W4AFP8 model with ep-moe mode", Modifications: Workflow and
+ * Kernel): routing ids -> permutation preprocess -> FP8 scaling of the hidden
+ * states -> int4 x FP8 grouped GEMM w13 (group size 128) -> SiLU and Mul with
+ * FP8 re-scaling -> grouped GEMM w2 -> unpermutation weighted by the routing
+ * weights.  The dense Linear is the same mixed-input GEMM with one weight
+ * matrix (lyraW4AFp8 page, "LyraW4fp8": W4AFP8 MoE and GEMMs).
+ *
+ * Conventions for every entry point below
+ *  - Pointers are DEVICE pointers owned by the caller, unless stated.  The
+ *    library never allocates, frees or synchronises; every call only enqueues
+ *    kernels on `stream` (a cudaStream_t; NULL = the legacy default stream)
+ *    and returns.  Results are valid once the stream has reached that point.
+ *  - Sizes are int64_t element counts.  bf16 tensors are passed as uint16_t
+ *    bit patterns.  All matrices are row-major and densely packed unless a
+ *    leading dimension is given.
+ *  - Return value: a w4a8_status.  Shapes, null pointers and alignment are
+ *    checked on the host before anything is launched (W4A8_ERR_INVALID_ARG /
+ *    W4A8_ERR_UNSUPPORTED, nothing enqueued).  A failed launch returns
+ *    W4A8_ERR_CUDA.  w4a8_last_error() gives a text for the calling thread.
+ *  - Device pointers passed to a GEMM must be 16-byte aligned (TMA).
+ *  - Calls on the same stream are ordered; calls on different streams that
+ *    share output buffers race.
+ *
+ * Packed weight layout (canonical): uint8 [E][N][K/2].  Byte b of a row
+ * holds element k = 2b in bits 0-3 and k = 2b+1 in bits 4-7, each a two's
+ * complement nibble in -8..7 (lower k in lower bits, the unpack order of the
+ * SGLang PR #37796 page, Modifications).  Weight scales: fp32 [E][K/128][N]
+ * (N contiguous, the [E, K/128, N] scale layout of the PR #37796 page).
+ * Activation scales: fp32 [K/128][ld], element (row m, group g) at
+ * scales[g*ld + m], ld >= M and ld % 4 == 0 (group-major, so a tile of rows of
+ * one group is contiguous for TMA).
+ */
+#ifndef W4A8MOE_H
+#define W4A8MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define W4A8MOE_ABI_VERSION 1
+
+typedef enum {
+  W4A8_OK = 0,
+  W4A8_ERR_INVALID_ARG = 1, /* bad shape, null or misaligned pointer, k > E, ...  */
+  W4A8_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels implement       */
+  W4A8_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed             */
+  W4A8_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up (see below)     */
+} w4a8_status;
+
+/* Static text of a status code. */
+const char* w4a8_status_string(int status);
+/* Detail of the last non-OK status returned on the calling host thread. */
+const char* w4a8_last_error(void);
+/* W4A8MOE_ABI_VERSION of the loaded library. */
+int w4a8_abi_version(void);
+
+/*
+ * Reads and clears the device-side error word of the current device
+ * (synchronises the device).  Non-zero means a kernel's bounded wait on an
+ * mbarrier gave up (W4A8_ERR_TIMEOUT) and that kernel's outputs are invalid.
+ * For tests and diagnostics, not for the hot path.
+ */
+int w4a8_device_error(void);
+
+/*
+ * (1) Router top-k.  For each token t: the k experts with the largest logits
+ * in descending order (equal logits: lower expert id first), and weights
+ * p_j = softmax(logits[t])_j; with renormalize != 0 the weights are divided by
+ * their sum over the selected experts, i.e. exp(l_j - l_max) / sum_sel.
+ * The ids are what the permutation preprocess of the PR #7762 page consumes
+ * (run_cutlass_moe_ep_preproess(topk_ids, ...)).
+ *   logits   fp32 [T][E]     topk_ids int32 [T][k]     topk_w fp32 [T][k]
+ *   1 <= k <= min(E, 32), 1 <= E <= 1024, T >= 0.  NaN logits: undefined order.
+ */
+int moe_route_topk(const float* logits, int64_t T, int64_t E, int k, int renormalize,
+                   int32_t* topk_ids, float* topk_w, void* stream);
+
+/*
+ * (2) Permutation preprocess (PR #7762 page, review of ep_moe/kernels.py:
+ * stable sort of the flat ids, seg_indptr[E+1] int64, src2dst int32).
+ * Flat pair f = t*k + j is routed to expert topk_ids[f].  Pairs are ordered by
+ * expert, and within an expert by ascending f (a stable sort).
+ *   seg_indptr int64 [E+1]: seg_indptr[e] = first sorted position of expert e,
+ *                           seg_indptr[E] = T*k.
+ *   src2dst    int32 [T*k]: sorted position of pair f.
+ *   dst2src    int32 [T*k]: pair at sorted position j (the inverse).
+ * Ids outside [0, E) make the kernel set the device error word (code 2) and
+ * the outputs undefined.  1 <= E <= 1024, T*k < 2^31.
+ * ws / ws_bytes: workspace of at least w4a8_workspace_bytes(W4A8_OP_PERMUTE,
+ * T*k, 0, 0, E) bytes (may be 0 and NULL when that is 0).
+ */
+int moe_permute(const int32_t* topk_ids, int64_t T, int k, int64_t E, int64_t* seg_indptr,
+                int32_t* src2dst, int32_t* dst2src, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * (3) FP8 E4M3 activation quantisation per token per group of 128 columns
+ * ("scale operations on the input hidden states", PR #7762 page, Cutlass W4A8
+ * MoE): amax = max|x| over the group, clamped to >= 1e-12 (DeepGEMM PR #53
+ * page: clamp amax before the reciprocal), s = amax / 448 (fp32 division),
+ * q = E4M3(x / s) (fp32 division; round to nearest even, saturating at +-448
+ * as on the PR #37796 page's fp8 write path).
+ * Optional gather: output row j reads input row (row_index[j] / row_div); with
+ * row_index = NULL output row j reads input row j and M_out must equal M_src.
+ * In the MoE this quantises the permuted copy directly (row_index = dst2src,
+ * row_div = k); quantisation is per row, so it equals permuting quantised rows.
+ *   x bf16 [M_src][K]   q uint8 [M_out][K]   scales fp32 [K/128][scale_ld]
+ *   K % 128 == 0, scale_ld >= M_out, scale_ld % 4 == 0.
+ */
+int fp8_quant_per_token_group(const uint16_t* x, int64_t M_src, int64_t K,
+                              const int32_t* row_index, int64_t row_div, int64_t M_out,
+                              uint8_t* q, float* scales, int64_t scale_ld, void* stream);
+
+/*
+ * (4) Grouped int4 x FP8 GEMM (PR #7762 page: CUTLASS W4A8 grouped GEMM,
+ * chunk_size 128).  For expert e and rows j in [seg_indptr[e], seg_indptr[e+1]):
+ *   C[j][n] = bf16( sum_g a_s[g][j] * b_s[e][g][n] *
+ *                   sum_{k in group g} e4m3(A[j][k]) * int4(B[e][n][k]) )
+ * accumulated in fp32 per group on the tensor cores and promoted in fp32.
+ *   A uint8 [M_total][K] (E4M3 codes)         a_scales fp32 [K/128][a_scale_ld]
+ *   B_packed uint8 [E][N][K/2] (canonical)    b_scales fp32 [E][K/128][N]
+ *   seg_indptr int64 [E+1] (device; seg_indptr[E] must equal M_total)
+ *   C bf16 [M_total][N]
+ *   K % 128 == 0, N % 128 == 0, 1 <= E <= 1024, M_total < 2^31.
+ * Rows outside every segment are not written.  ws may be NULL (none needed).
+ */
+int w4a8_grouped_gemm(const uint8_t* A, const float* a_scales, int64_t a_scale_ld,
+                      const uint8_t* B_packed, const float* b_scales, const int64_t* seg_indptr,
+                      int64_t E, int64_t N, int64_t K, int64_t M_total, uint16_t* C, void* ws,
+                      size_t ws_bytes, void* stream);
+
+/*
+ * (5) SiLU and Mul with FP8 re-quantisation of the intermediate (PR #7762
+ * page: "handling SiLU and Mul activation functions", scale operations on the
+ * intermediate values).  gate_up row m holds gate in columns [0, I) and up in
+ * [I, 2I); h = silu(gate) * up = gate / (1 + exp(-gate)) * up in fp32, then
+ * the quantisation of (3) on h.
+ *   gate_up bf16 [M][2I]   q uint8 [M][I]   scales fp32 [I/128][scale_ld]
+ *   I % 128 == 0, scale_ld >= M, scale_ld % 4 == 0.
+ */
+int silu_mul_requant(const uint16_t* gate_up, int64_t M, int64_t I, uint8_t* q, float* scales,
+                     int64_t scale_ld, void* stream);
+
+/*
+ * (6) Unpermute and combine (PR #7762 page: post-reordering of the outputs):
+ *   out[t][c] = bf16( sum_{j=0..k-1} topk_w[t][j] * Y[src2dst[t*k+j]][c] ),
+ * fp32 accumulation in j order.
+ *   Y bf16 [T*k][H]   src2dst int32 [T*k]   topk_w fp32 [T][k]   out bf16 [T][H]
+ *   H % 8 == 0.
+ */
+int moe_unpermute_combine(const uint16_t* Y, const int32_t* src2dst, const float* topk_w,
+                          int64_t T, int k, int64_t H, uint16_t* out, void* stream);
+
+/*
+ * (7) Dense W4AFP8 Linear: (4) with one weight matrix and no routing
+ * (lyraW4AFp8 page: Machete mixed-input GEMM for the Linear layers).
+ *   A uint8 [M][K]   a_scales fp32 [K/128][a_scale_ld]
+ *   B_packed uint8 [N][K/2]   b_scales fp32 [K/128][N]   C bf16 [M][N]
+ *   K % 128 == 0, N % 128 == 0.
+ * ws: at least w4a8_workspace_bytes(W4A8_OP_LINEAR, M, N, K, 1) bytes (the
+ * split-K partial sums of small-M shapes); may be NULL when that is 0.
+ */
+int w4a8_linear(const uint8_t* A, const float* a_scales, int64_t a_scale_ld,
+                const uint8_t* B_packed, const float* b_scales, int64_t M, int64_t N, int64_t K,
+                uint16_t* C, void* ws, size_t ws_bytes, void* stream);
+
+/* Operation ids for w4a8_workspace_bytes. */
+#define W4A8_OP_PERMUTE 1
+#define W4A8_OP_GROUPED_GEMM 2
+#define W4A8_OP_LINEAR 3
+
+/* Workspace (bytes) an operation needs for the given shape; 0 = none. */
+size_t w4a8_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int64_t E);
+
+/*
+ * The whole layer in one call: (1) route -> (2) permute -> (3) quantise the
+ * permuted hidden states -> (4) w13 -> (5) SiLU and Mul + requantise -> (4) w2
+ * -> (6) combine.  Seven launches (plus the permutation's), nothing else.
+ *   x bf16 [T][H]   logits fp32 [T][E]
+ *   w13 uint8 [E][2I][H/2] (rows [0, I) gate, [I, 2I) up)   w13_s fp32 [E][H/128][2I]
+ *   w2 uint8 [E][H][I/2]   w2_s fp32 [E][I/128][H]          out bf16 [T][H]
+ *   ws: w4a8_moe_workspace_bytes(T, H, I, E, k) bytes, 256-byte aligned; it
+ *   holds the intermediates (ids, weights, permutation, FP8 codes and scales,
+ *   Y13, Y2), whose offsets are given by w4a8_moe_workspace_layout.
+ */
+int w4a8_moe_forward(const uint16_t* x, const float* logits, int64_t T, int64_t H, int64_t I,
+                     int64_t E, int k, int renormalize, const uint8_t* w13, const float* w13_s,
+                     const uint8_t* w2, const float* w2_s, uint16_t* out, void* ws,
+                     size_t ws_bytes, void* stream);
+size_t w4a8_moe_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int k);
+
+/* Byte offsets of the intermediates inside the w4a8_moe_forward workspace. */
+typedef struct {
+  size_t topk_ids, topk_w, seg_indptr, src2dst, dst2src, xq, xs, y13, hq, hs, y2, permute_ws;
+  int64_t scale_ld; /* leading dimension of xs and hs: T*k rounded up to 4 */
+  size_t total;
+} w4a8_moe_layout;
+int w4a8_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, int k,
+                              w4a8_moe_layout* layout /* host pointer */);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* W4A8MOE_H */

@@ -152,3 +152,60 @@ def expert_scales(seed: int, stream: int, E: int, N: int, K: int, experts) -> di
     G = K // 128
     per = G * N
     return {int(e): scales(seed, stream, int(e) * per, per).reshape(G, N) for e in experts}
+
+
+# ----------------------------------------------------------------------------
+# Device twin (inputs/gen.cu): the same streams, filled on the GPU.
+
+import os as _os  # noqa: E402
+
+_GEN_SRC = _os.path.join(_os.path.dirname(_os.path.abspath(__file__)), "gen.cu")
+_GEN_LIB = _os.path.join(_os.path.dirname(_os.path.abspath(__file__)), "_lib", "libw4a8gen.so")
+_gen = None
+
+
+def build_gen() -> str:
+    from w4afp8_mixture_experts_gb300.build import build_shared
+    return build_shared([_GEN_SRC], _GEN_LIB, [])
+
+
+def _genlib():
+    global _gen
+    if _gen is None:
+        import ctypes
+        if not _os.path.exists(_GEN_LIB):
+            raise RuntimeError(f"{_GEN_LIB} is missing: run inputs.build_gen()")
+        lib = ctypes.CDLL(_GEN_LIB)
+        lib.w4a8gen_fill_int4.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_uint64,
+                                          ctypes.c_uint32, ctypes.c_void_p]
+        lib.w4a8gen_fill_scales.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_uint64,
+                                            ctypes.c_uint32, ctypes.c_float, ctypes.c_float, ctypes.c_void_p]
+        _gen = lib
+    return _gen
+
+
+def gpu_packed_int4(seed: int, stream: int, shape, device="cuda", start: int = 0):
+    """torch uint8 tensor of `shape` on the GPU: bytes start.. of the stream."""
+    import ctypes
+
+    import torch
+    t = torch.empty(shape, dtype=torch.uint8, device=device)
+    st = ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+    rc = _genlib().w4a8gen_fill_int4(ctypes.c_void_p(t.data_ptr()), start, t.numel(), seed, stream, st)
+    if rc:
+        raise RuntimeError(f"w4a8gen_fill_int4 failed ({rc})")
+    return t
+
+
+def gpu_scales(seed: int, stream: int, shape, device="cuda", start: int = 0):
+    """torch fp32 tensor of `shape` on the GPU: scales start.. of the stream."""
+    import ctypes
+
+    import torch
+    t = torch.empty(shape, dtype=torch.float32, device=device)
+    st = ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+    rc = _genlib().w4a8gen_fill_scales(ctypes.c_void_p(t.data_ptr()), start, t.numel(), seed, stream,
+                                       float(SCALE_LO), float(SCALE_SPAN), st)
+    if rc:
+        raise RuntimeError(f"w4a8gen_fill_scales failed ({rc})")
+    return t

@@ -1,0 +1,103 @@
+"""GPU parity of the int4 x FP8 grouped GEMM and the dense Linear (tcgen05 kernels).
+
+Inputs are seeded; the oracle computes in float64 from the same E4M3 codes,
+int4 values and fp32 scales, and its result is rounded once to bf16.  Each
+GEMM stage must agree within a relative Frobenius error of 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import inputs
+import oracle
+from oracle import e4m3
+from gpu_util import f64_of_bf16, rel_fro, scales_to_gpu_layout, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _acts(rng, M, K):
+    x = rng.standard_normal((M, K)).astype(np.float32) * rng.uniform(0.1, 10, (M, 1)).astype(np.float32)
+    return oracle.quant_per_token_group(x)
+
+
+def _weights(rng, E, N, K):
+    packed = rng.integers(0, 256, size=(E, N, K // 2), dtype=np.uint8)
+    s = rng.uniform(0.005, 0.02, size=(E, K // 128, N)).astype(np.float32)
+    return packed, s
+
+
+def _run_grouped(lib, aq, a_s, packed, ws, seg):
+    E, N, _ = packed.shape
+    return lib.w4a8_grouped_gemm(to_dev(aq), scales_to_gpu_layout(a_s), to_dev(packed), to_dev(ws),
+                                 to_dev(seg.astype(np.int64)))
+
+
+def _oracle_grouped(aq, a_s, packed, ws, seg):
+    return oracle.round_bf16(oracle.grouped_gemm(aq, a_s, seg, lambda e: oracle.unpack_int4(packed[e]),
+                                                 lambda e: ws[e].T))
+
+
+def test_integer_case_is_exact(lib):
+    # all scales 1, activations small integers, weights in {-1, 0, 1}: every product and
+    # partial sum is an exact integer in fp32, so the device result must be exact.
+    rng = np.random.default_rng(1)
+    M, N, K = 40, 256, 256
+    a_int = rng.integers(-3, 4, size=(M, K))
+    aq = e4m3.encode(a_int.astype(np.float32))
+    a_s = np.ones((M, K // 128), np.float32)
+    w = rng.integers(-1, 2, size=(1, N, K))
+    packed = oracle.pack_int4(w)
+    ws = np.ones((1, K // 128, N), np.float32)
+    seg = np.array([0, M])
+    got = f64_of_bf16(_run_grouped(lib, aq, a_s, packed, ws, seg))
+    ref = oracle.round_bf16(a_int.astype(np.float64) @ w[0].T.astype(np.float64))
+    assert np.array_equal(got, ref)
+
+
+def test_every_int4_value(lib):
+    # one-hot activations pick single weights: C[j][n] = a * int4(W[n][j]) exactly
+    M, N, K = 128, 128, 128
+    aq = np.zeros((M, K), np.uint8)
+    aq[np.arange(M), np.arange(M)] = e4m3.encode(np.float32(2.0))
+    a_s = np.ones((M, 1), np.float32)
+    rng = np.random.default_rng(2)
+    w = rng.integers(-8, 8, size=(1, N, K))
+    w[0, :16, :16] = np.arange(-8, 8)[None, :]
+    packed = oracle.pack_int4(w)
+    ws = np.ones((1, 1, N), np.float32)
+    got = f64_of_bf16(_run_grouped(lib, aq, a_s, packed, ws, np.array([0, M])))
+    assert np.array_equal(got, 2.0 * w[0].T.astype(np.float64))
+
+
+@pytest.mark.parametrize("counts,N,K", [
+    ([3, 0, 17, 1, 64, 2, 0, 9], 256, 256),          # decode-style tile (few rows per expert)
+    ([40, 200, 0, 129, 5, 300, 1, 77], 384, 512),    # several token chunks per expert
+    ([1] * 37, 128, 1024),
+    ([0, 0, 0, 500], 128, 128),
+])
+def test_grouped_gemm(lib, counts, N, K):
+    rng = np.random.default_rng(sum(counts) + N + K)
+    E = len(counts)
+    seg = np.concatenate([[0], np.cumsum(counts)])
+    M = int(seg[-1])
+    aq, a_s = _acts(rng, M, K)
+    packed, ws = _weights(rng, E, N, K)
+    got = f64_of_bf16(_run_grouped(lib, aq, a_s, packed, ws, seg))
+    ref = _oracle_grouped(aq, a_s, packed, ws, seg)
+    err = rel_fro(got, ref)
+    assert err <= 1e-3, (err, np.abs(got - ref).max())
+    assert lib.device_error() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (16, 256, 1536), (128, 384, 512), (300, 128, 2048),
+                                   (1000, 256, 256)])
+def test_linear(lib, M, N, K):
+    rng = np.random.default_rng(M * 7 + N + K)
+    aq, a_s = _acts(rng, M, K)
+    packed, ws = _weights(rng, 1, N, K)
+    got = f64_of_bf16(lib.w4a8_linear(to_dev(aq), scales_to_gpu_layout(a_s), to_dev(packed[0]), to_dev(ws[0])))
+    ref = oracle.linear(aq, a_s, oracle.unpack_int4(packed[0]), ws[0].T)
+    err = rel_fro(got, ref)
+    assert err <= 1e-3, (err, np.abs(got - ref).max())
+    assert lib.device_error() == 0

@@ -1,0 +1,150 @@
+"""GPU parity of the routing, permutation, quantisation, SiLU-requant and combine kernels.
+
+Each kernel runs through the C ABI (the Python binding only marshals) and is
+compared element by element with the CPU oracle on the same seeded inputs.
+"""
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import inputs
+import oracle
+from gpu_util import (bf16_from_bits, bf16_ulp_diff, bits_of_bf16, f64_of_bf16, rel_fro,
+                      scales_from_gpu_layout, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+def test_generator_twin_is_bit_exact(lib):
+    for seed, stream, start, n in [(0, 1, 0, 4099), (3, 2, 12345, 1000), (7, 4, 1 << 33, 517)]:
+        g = inputs.gpu_packed_int4(seed, stream, (n,), start=start).cpu().numpy()
+        assert np.array_equal(g, inputs.packed_int4(seed, stream, start, n))
+        s = inputs.gpu_scales(seed, stream, (n,), start=start).cpu().numpy()
+        assert np.array_equal(s, inputs.scales(seed, stream, start, n))
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 8, 2), (333, 8, 2), (64, 256, 8), (257, 384, 8), (40, 1000, 32),
+                                   (17, 5, 5), (9, 33, 1)])
+@pytest.mark.parametrize("renorm", [True, False])
+def test_route_topk(lib, T, E, k, renorm):
+    rng = np.random.default_rng(T * 1000 + E + k)
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    lg[0, : min(E, 6)] = lg[0, 0]  # ties
+    if T > 3:
+        lg[3] = np.round(lg[3])    # many ties
+    ids, w = lib.moe_route_topk(to_dev(lg), k, renorm)
+    rid, rw = oracle.route_topk(lg, k, renorm)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    got = w.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(got - rw) / np.abs(rw)) <= 1e-6
+
+
+def _distinct_ids(rng, T, E, k, skew=None):
+    ids = np.empty((T, k), np.int32)
+    for t in range(T):
+        if skew is not None:
+            p = skew / skew.sum()
+            ids[t] = rng.choice(E, size=k, replace=False, p=p)
+        else:
+            ids[t] = rng.choice(E, size=k, replace=False)
+    return ids
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 1, 1), (5, 8, 2), (64, 256, 8), (1000, 384, 8), (4096, 16, 4),
+                                   (2049, 1024, 3)])
+def test_permute(lib, T, E, k):
+    rng = np.random.default_rng(T + E + k)
+    ids = _distinct_ids(rng, T, E, k)
+    seg, s2d, d2s = lib.moe_permute(to_dev(ids), E)
+    rs, rs2d, rd2s = oracle.permute(ids, E)
+    assert np.array_equal(seg.cpu().numpy(), rs)
+    assert np.array_equal(s2d.cpu().numpy(), rs2d)
+    assert np.array_equal(d2s.cpu().numpy(), rd2s)
+
+
+def test_permute_skewed_and_empty(lib):
+    rng = np.random.default_rng(5)
+    E = 64
+    skew = np.zeros(E)
+    skew[[3, 7, 8, 40, 41, 42, 63]] = [100, 1, 1, 5, 5, 5, 30]
+    ids = _distinct_ids(rng, 3000, E, 4, skew)
+    seg, s2d, d2s = lib.moe_permute(to_dev(ids), E)
+    rs, rs2d, rd2s = oracle.permute(ids, E)
+    assert np.array_equal(seg.cpu().numpy(), rs)
+    assert np.array_equal(s2d.cpu().numpy(), rs2d)
+    assert np.array_equal(d2s.cpu().numpy(), rd2s)
+
+
+def _bf16_rows(rng, M, K):
+    x = rng.standard_normal((M, K)).astype(np.float32) * rng.uniform(0.01, 30, (M, 1)).astype(np.float32)
+    if M > 2:
+        x[1] = 0.0                              # all-zero row
+        x[2, 5] = 3.0e4                         # a spike
+    if M > 4:
+        x[4, :] = np.float32(1e-30)             # tiny values
+    return inputs.to_bf16_bits(x)
+
+
+@pytest.mark.parametrize("M,K", [(1, 128), (37, 256), (300, 7168), (1024, 2048)])
+def test_quant(lib, M, K):
+    rng = np.random.default_rng(M + K)
+    xb = _bf16_rows(rng, M, K)
+    q, s = lib.fp8_quant_per_token_group(bf16_from_bits(xb))
+    rq, rs = oracle.quant_per_token_group(inputs.bf16_bits_to_f32(xb))
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert np.array_equal(scales_from_gpu_layout(s, M), rs)
+
+
+def test_quant_gather(lib):
+    rng = np.random.default_rng(9)
+    T, K, k = 50, 512, 3
+    xb = _bf16_rows(rng, T, K)
+    ids = _distinct_ids(rng, T, 16, k)
+    _, _, d2s = oracle.permute(ids, 16)
+    q, s = lib.fp8_quant_per_token_group(bf16_from_bits(xb), to_dev(d2s.astype(np.int32)), k)
+    rq, rs = oracle.quant_per_token_group(inputs.bf16_bits_to_f32(xb))
+    tok = d2s // k
+    assert np.array_equal(q.cpu().numpy(), rq[tok])
+    assert np.array_equal(scales_from_gpu_layout(s, T * k), rs[tok])
+
+
+@pytest.mark.parametrize("M,I", [(3, 128), (77, 512), (512, 2048)])
+def test_silu_mul_requant(lib, M, I):
+    # Codes are decided in fp32 on both sides, but exp differs in the last bit between the
+    # device and numpy, so a code may move by one step on a rounding tie.
+    rng = np.random.default_rng(M + I)
+    gu = rng.standard_normal((M, 2 * I)).astype(np.float32) * 4
+    gu[0, :I] = 0.0
+    if M > 1:
+        gu[1, :I] = -200.0                      # silu(-200) ~ 0
+    gub = inputs.to_bf16_bits(gu)
+    q, s = lib.silu_mul_requant(bf16_from_bits(gub))
+    rq, rs = oracle.silu_mul_requant(inputs.bf16_bits_to_f32(gub).astype(np.float64))
+    gq = q.cpu().numpy()
+    gs = scales_from_gpu_layout(s, M)
+    assert np.max(np.abs(gs.astype(np.float64) - rs) / rs) <= 1e-6
+    diff = gq != rq
+    assert diff.mean() <= 1e-3
+    if diff.any():
+        step = np.abs(gq[diff].astype(np.int32) - rq[diff].astype(np.int32))
+        assert np.all((step == 1) | ((gq[diff] & 0x7F) == 0) & ((rq[diff] & 0x7F) <= 1))
+    assert rel_fro(oracle.dequant(gq, gs), oracle.dequant(rq, rs)) <= 1e-3
+
+
+@pytest.mark.parametrize("T,k,H", [(1, 1, 8), (64, 8, 7168), (300, 2, 256), (129, 32, 64)])
+def test_combine(lib, T, k, H):
+    rng = np.random.default_rng(T + k + H)
+    P = T * k
+    yb = inputs.to_bf16_bits(rng.standard_normal((P, H)).astype(np.float32))
+    s2d = rng.permutation(P).astype(np.int32)
+    w = rng.uniform(0, 1, (T, k)).astype(np.float32)
+    w /= w.sum(1, keepdims=True)
+    out = lib.moe_unpermute_combine(bf16_from_bits(yb), to_dev(s2d), to_dev(w))
+    ref = oracle.round_bf16(oracle.unpermute_combine(inputs.bf16_bits_to_f32(yb), s2d, w, T, k))
+    gb = bits_of_bf16(out)
+    rb = oracle.bf16_bits(ref)
+    ulp = bf16_ulp_diff(gb, rb)
+    assert ulp.max() <= 1 and (ulp > 0).mean() <= 1e-2
+    assert rel_fro(f64_of_bf16(out), ref) <= 1e-3

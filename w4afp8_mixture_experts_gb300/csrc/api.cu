@@ -1,0 +1,160 @@
+// Status plumbing, workspace sizing and the whole-layer entry point.
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+
+namespace w4a8 {
+
+namespace {
+thread_local char g_msg[512] = "";
+std::vector<device_error_reader>& readers() {
+  static std::vector<device_error_reader> v;
+  return v;
+}
+std::mutex g_mu;
+}  // namespace
+
+int set_error(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+int check_launch(const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(W4A8_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return W4A8_OK;
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cache[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 148;
+  }
+  return cache[dev];
+}
+
+void register_device_error_reader(device_error_reader f) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  readers().push_back(f);
+}
+
+namespace {
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+int layout_of(int64_t T, int64_t H, int64_t I, int64_t E, int k, w4a8_moe_layout* L) {
+  W4A8_REQUIRE(T >= 0 && H > 0 && I > 0 && E >= 1 && k >= 1, "bad layer shape");
+  W4A8_REQUIRE(H % 128 == 0 && I % 128 == 0, "H and I must be multiples of 128");
+  const int64_t P = T * k;
+  const int64_t ld = (P + 3) / 4 * 4 > 0 ? (P + 3) / 4 * 4 : 4;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  L->topk_ids = take(P * 4);
+  L->topk_w = take(P * 4);
+  L->seg_indptr = take((E + 1) * 8);
+  L->src2dst = take(P * 4);
+  L->dst2src = take(P * 4);
+  L->xq = take(P * H);
+  L->xs = take((H / 128) * ld * 4);
+  L->y13 = take(P * 2 * I * 2);
+  L->hq = take(P * I);
+  L->hs = take((I / 128) * ld * 4);
+  L->y2 = take(P * H * 2);
+  L->permute_ws = take(0);
+  L->scale_ld = ld;
+  L->total = o;
+  return W4A8_OK;
+}
+}  // namespace
+
+}  // namespace w4a8
+
+extern "C" const char* w4a8_status_string(int status) {
+  switch (status) {
+    case W4A8_OK: return "ok";
+    case W4A8_ERR_INVALID_ARG: return "invalid argument";
+    case W4A8_ERR_UNSUPPORTED: return "unsupported";
+    case W4A8_ERR_CUDA: return "CUDA error";
+    case W4A8_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+extern "C" const char* w4a8_last_error(void) { return w4a8::g_msg; }
+
+extern "C" int w4a8_abi_version(void) { return W4A8MOE_ABI_VERSION; }
+
+extern "C" int w4a8_device_error(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  int v = 0;
+  std::lock_guard<std::mutex> lk(w4a8::g_mu);
+  for (auto f : w4a8::readers()) v |= f();
+  return v;
+}
+
+extern "C" size_t w4a8_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int64_t E) {
+  (void)op;
+  (void)M;
+  (void)N;
+  (void)K;
+  (void)E;
+  return 0;
+}
+
+extern "C" int w4a8_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, int k,
+                                         w4a8_moe_layout* layout) {
+  if (!layout) return w4a8::set_error(W4A8_ERR_INVALID_ARG, "layout is null");
+  return w4a8::layout_of(T, H, I, E, k, layout);
+}
+
+extern "C" size_t w4a8_moe_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int k) {
+  w4a8_moe_layout L;
+  if (w4a8::layout_of(T, H, I, E, k, &L) != W4A8_OK) return 0;
+  return L.total;
+}
+
+extern "C" int w4a8_moe_forward(const uint16_t* x, const float* logits, int64_t T, int64_t H, int64_t I, int64_t E,
+                                int k, int renormalize, const uint8_t* w13, const float* w13_s, const uint8_t* w2,
+                                const float* w2_s, uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+  using namespace w4a8;
+  w4a8_moe_layout L;
+  int rc = layout_of(T, H, I, E, k, &L);
+  if (rc) return rc;
+  W4A8_REQUIRE(ws != nullptr && ws_bytes >= L.total, "workspace too small: need %zu bytes", L.total);
+  W4A8_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255) == 0, "workspace must be 256-byte aligned");
+  if (T == 0) return W4A8_OK;
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  int32_t* ids = reinterpret_cast<int32_t*>(b + L.topk_ids);
+  float* tw = reinterpret_cast<float*>(b + L.topk_w);
+  int64_t* seg = reinterpret_cast<int64_t*>(b + L.seg_indptr);
+  int32_t* s2d = reinterpret_cast<int32_t*>(b + L.src2dst);
+  int32_t* d2s = reinterpret_cast<int32_t*>(b + L.dst2src);
+  uint8_t* xq = b + L.xq;
+  float* xs = reinterpret_cast<float*>(b + L.xs);
+  uint16_t* y13 = reinterpret_cast<uint16_t*>(b + L.y13);
+  uint8_t* hq = b + L.hq;
+  float* hs = reinterpret_cast<float*>(b + L.hs);
+  uint16_t* y2 = reinterpret_cast<uint16_t*>(b + L.y2);
+  const int64_t P = T * k;
+  if ((rc = moe_route_topk(logits, T, E, k, renormalize, ids, tw, stream))) return rc;
+  if ((rc = moe_permute(ids, T, k, E, seg, s2d, d2s, nullptr, 0, stream))) return rc;
+  if ((rc = fp8_quant_per_token_group(x, T, H, d2s, k, P, xq, xs, L.scale_ld, stream))) return rc;
+  if ((rc = w4a8_grouped_gemm(xq, xs, L.scale_ld, w13, w13_s, seg, E, 2 * I, H, P, y13, nullptr, 0, stream)))
+    return rc;
+  if ((rc = silu_mul_requant(y13, P, I, hq, hs, L.scale_ld, stream))) return rc;
+  if ((rc = w4a8_grouped_gemm(hq, hs, L.scale_ld, w2, w2_s, seg, E, H, I, P, y2, nullptr, 0, stream))) return rc;
+  return moe_unpermute_combine(y2, s2d, tw, T, k, H, out, stream);
+}
