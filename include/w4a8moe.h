@@ -197,6 +197,29 @@ int w4a8_moe_forward(const uint16_t* x, const float* logits, int64_t T, int64_t 
                      size_t ws_bytes, void* stream);
 size_t w4a8_moe_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int k);
 
+/*
+ * w4a8_moe_forward without a workspace: for callers that cannot allocate
+ * device memory, such as a plugin whose host application owns the device
+ * allocator and passes in only the layer's inputs and outputs, or a C program
+ * that must not allocate after start-up.  The pages have no counterpart of
+ * this call; it exists for those callers.
+ *   Same arguments as w4a8_moe_forward, minus ws / ws_bytes.  The
+ *   intermediates live in a fixed array of w4a8_moe_noalloc_scratch_bytes()
+ *   (64 MiB) inside the library, which every GPU that loads the library keeps
+ *   until the process exits.  A layer whose w4a8_moe_workspace_bytes() exceeds
+ *   that is rejected with W4A8_ERR_INVALID_ARG before anything is launched.
+ *   The call itself never calls cudaMalloc / cudaFree or any allocating routine.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.  All calls share the one array and it keeps the
+ *   last call's contents: calls that overlap on the GPU (other streams, other
+ *   host threads) race and corrupt each other; order them on one stream.
+ */
+int w4a8_moe_forward_noalloc(const uint16_t* x, const float* logits, int64_t T, int64_t H, int64_t I,
+                             int64_t E, int k, int renormalize, const uint8_t* w13, const float* w13_s,
+                             const uint8_t* w2, const float* w2_s, uint16_t* out, void* stream);
+size_t w4a8_moe_noalloc_scratch_bytes(void);
+
 /* Byte offsets of the intermediates inside the w4a8_moe_forward workspace. */
 typedef struct {
   size_t topk_ids, topk_w, seg_indptr, src2dst, dst2src, xq, xs, y13, hq, hs, y2, permute_ws;

@@ -38,6 +38,9 @@ _SIGS = {
     "w4a8_moe_forward": (_c_int, [_c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_vp,
                                   _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]),
     "w4a8_moe_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_i64, _c_i64, _c_int]),
+    "w4a8_moe_forward_noalloc": (_c_int, [_c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_vp,
+                                          _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "w4a8_moe_noalloc_scratch_bytes": (_c_sz, []),
 }
 
 
@@ -229,6 +232,21 @@ def w4a8_moe_forward(x, logits, k: int, w13, w13_s, w2, w2_s, renormalize: bool 
         out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
     _check(load().w4a8_moe_forward(_p(x), _p(logits), T, H, I, E, k, int(bool(renormalize)), _p(w13), _p(w13_s),
                                    _p(w2), _p(w2_s), _p(out), _p(ws), ws.numel(), _stream()))
+    return out
+
+
+def w4a8_moe_forward_noalloc(x, logits, k: int, w13, w13_s, w2, w2_s, out, renormalize: bool = True):
+    """The whole layer into a caller-given `out`, with the intermediates kept in the
+    library's fixed device array instead of a workspace (for callers that cannot
+    allocate device memory).  Calls that overlap on the GPU race on that array."""
+    _req(x, torch.bfloat16, "x", 2)
+    _req(logits, torch.float32, "logits", 2)
+    _req(out, torch.bfloat16, "out", 2)
+    T, H = x.shape
+    E = logits.shape[1]
+    I = w13.shape[1] // 2
+    _check(load().w4a8_moe_forward_noalloc(_p(x), _p(logits), T, H, I, E, k, int(bool(renormalize)), _p(w13),
+                                           _p(w13_s), _p(w2), _p(w2_s), _p(out), _stream()))
     return out
 
 
