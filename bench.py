@@ -55,7 +55,7 @@ def parse():
 
 
 def load_peaks():
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")  # driver-written on the GPU pool
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
@@ -75,6 +75,9 @@ def get_workload(spec):
     if spec.startswith("linear"):
         M, N, K = (int(v) for v in spec.split(":")[1].split(","))
         return "linear", dict(M=M, N=N, K=K)
+    if spec.startswith("moe:"):  # moe:T,H,I,E,k  (custom shape, e.g. small profiling cases)
+        T, H, I, E, k = (int(v) for v in spec.split(":")[1].split(","))
+        return "moe", dict(T=T, H=H, I=I, E=E, k=k, zipf=None)
     return spec, dict(inputs.WORKLOADS[spec])
 
 

@@ -38,11 +38,12 @@ def _oracle_grouped(aq, a_s, packed, ws, seg):
                                                  lambda e: ws[e].T))
 
 
-def test_integer_case_is_exact(lib):
+@pytest.mark.parametrize("M", [16, 40, 300])  # M <= 32 per expert selects the small-M pipeline
+def test_integer_case_is_exact(lib, M):
     # all scales 1, activations small integers, weights in {-1, 0, 1}: every product and
     # partial sum is an exact integer in fp32, so the device result must be exact.
-    rng = np.random.default_rng(1)
-    M, N, K = 40, 256, 256
+    rng = np.random.default_rng(M)
+    N, K = 256, 256
     a_int = rng.integers(-3, 4, size=(M, K))
     aq = e4m3.encode(a_int.astype(np.float32))
     a_s = np.ones((M, K // 128), np.float32)
@@ -55,9 +56,10 @@ def test_integer_case_is_exact(lib):
     assert np.array_equal(got, ref)
 
 
-def test_every_int4_value(lib):
+@pytest.mark.parametrize("M", [13, 128])
+def test_every_int4_value(lib, M):
     # one-hot activations pick single weights: C[j][n] = a * int4(W[n][j]) exactly
-    M, N, K = 128, 128, 128
+    N, K = 128, 128
     aq = np.zeros((M, K), np.uint8)
     aq[np.arange(M), np.arange(M)] = e4m3.encode(np.float32(2.0))
     a_s = np.ones((M, 1), np.float32)
@@ -67,7 +69,7 @@ def test_every_int4_value(lib):
     packed = oracle.pack_int4(w)
     ws = np.ones((1, 1, N), np.float32)
     got = f64_of_bf16(_run_grouped(lib, aq, a_s, packed, ws, np.array([0, M])))
-    assert np.array_equal(got, 2.0 * w[0].T.astype(np.float64))
+    assert np.array_equal(got, 2.0 * w[0].T[:M].astype(np.float64))
 
 
 @pytest.mark.parametrize("counts,N,K", [

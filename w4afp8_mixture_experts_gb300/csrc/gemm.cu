@@ -45,13 +45,15 @@ namespace {
 
 constexpr int kBM = 128;      // weight rows per tile (MMA M)
 constexpr int kKStep = 32;    // K per tcgen05.mma for 8-bit operands
-constexpr int kWarps = 14;
-constexpr int kThreads = kWarps * 32;
 constexpr int kWarpTma = 0;
-constexpr int kWarpMma = 1;
-constexpr int kWarpEpi0 = 6;
-constexpr int kConvWarps = 4;
+constexpr int kConvSets = 2;                 // group sets: set c takes the groups with it % 2 == c
+constexpr int kWarpMma = 1;                  // warps 1 .. kConvSets issue the MMAs of one set each
+constexpr int kWarpConv0 = kWarpMma + kConvSets;
+constexpr int kConvWarps = 4;                // converter warps per set: one per tensor-memory lane quarter
+constexpr int kWarpEpi0 = kWarpConv0 + kConvSets * kConvWarps;
 constexpr int kEpiWarps = 8;
+constexpr int kWarps = kWarpEpi0 + kEpiWarps;
+constexpr int kThreads = kWarps * 32;
 constexpr int kMaxExperts = 1024;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s: no legitimate wait comes close
 
@@ -63,33 +65,37 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
   return p;
 }
 
-template <int NMAX_, int STAGES_, int ABUF_, bool A_TMEM_>
+template <int NMAX_, int STAGES_, int SSTAGES_, int ABUF_, int NP_, bool A_TMEM_>
 struct Cfg {
-  static constexpr int NMAX = NMAX_;
-  static constexpr int STAGES = STAGES_;
-  static constexpr int ABUF = ABUF_;
-  static constexpr bool A_TMEM = A_TMEM_;
+  static constexpr int NMAX = NMAX_;        // token tile (MMA N upper bound)
+  static constexpr int STAGES = STAGES_;    // main ring: token tile + packed weights
+  static constexpr int SSTAGES = SSTAGES_;  // scale ring: token + weight scales (epilogue only)
+  static constexpr int ABUF = ABUF_;        // converted weight buffers
+  static constexpr int NP = NP_;            // fp32 partial-product buffers in tensor memory
+  static constexpr bool A_TMEM = A_TMEM_;   // converted weights in tensor memory (else shared)
   static constexpr int kTokBytes = NMAX * 128;            // NMAX rows x 128 B, 128B swizzle
   static constexpr int kWpkBytes = kBM * 64;              // 128 rows x 64 B packed int4
   static constexpr int kABytes = kBM * 128;               // 128 rows x 128 B E4M3
-  static constexpr int kTscFloats = NMAX + 4;             // token scales, x rounded down to 4
-  static constexpr int kTscStride = (kTscFloats * 4 + 127) / 128 * 32;  // floats per stage, 128-B aligned
+  static constexpr int kWscOff = (NMAX * 4 + 127) / 128 * 128;          // weight scales in a slot
+  static constexpr int kScBytes = kWscOff + kBM * 4;                      // one scale slot (128-B aligned)
   static constexpr int kOffTok = 0;
   static constexpr int kOffWpk = kOffTok + STAGES * kTokBytes;
   static constexpr int kOffA = kOffWpk + STAGES * kWpkBytes;
-  static constexpr int kOffTsc = kOffA + (A_TMEM ? 0 : ABUF * kABytes);
-  static constexpr int kOffWsc = kOffTsc + STAGES * kTscStride * 4;
-  static constexpr int kOffBar = (kOffWsc + STAGES * kBM * 4 + 7) / 8 * 8;
-  static constexpr int kNumBars = 2 * STAGES + 2 * ABUF + 4;
+  static constexpr int kOffSc = kOffA + (A_TMEM ? 0 : ABUF * kABytes);
+  static constexpr int kOffBar = kOffSc + SSTAGES * kScBytes;
+  static constexpr int kNumBars = 2 * STAGES + 2 * SSTAGES + 2 * ABUF + NP;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffSched = kOffMisc + 64;
   static constexpr int kSmemBytes = kOffSched + 2 * (kMaxExperts + 1) * 4 + 1024;
-  static constexpr int kAColBase = 2 * NMAX;              // first tensor-memory column of A
-  static constexpr uint32_t kTmemCols = pow2_at_least(2 * NMAX + (A_TMEM ? ABUF * 32 : 0));
-  static_assert(NMAX % 16 == 0 && NMAX >= 16 && NMAX <= 128, "token tile");
+  static constexpr int kAColBase = NP * NMAX;             // first tensor-memory column of A
+  static constexpr uint32_t kTmemCols = pow2_at_least(NP * NMAX + (A_TMEM ? ABUF * 32 : 0));
+  static constexpr int kChunkMax = NMAX - 3;              // rows of a chunk (tile starts 4-aligned)
+  static_assert(NMAX % 16 == 0 && NMAX >= 16 && NMAX <= 256, "token tile");
   static_assert(kTokBytes % 1024 == 0 && kOffWpk % 1024 == 0 && kOffA % 1024 == 0, "alignment");
-  static_assert(kTmemCols <= 512, "tensor memory");
+  static_assert(NP * NMAX + (A_TMEM ? ABUF * 32 : 0) <= 512, "tensor memory");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(ABUF % kConvSets == 0 && NP % kConvSets == 0, "each set owns every kConvSets-th buffer");
+  static_assert(NP <= ABUF, "an A-buffer completion barrier must not run a phase ahead of the epilogue");
 };
 
 struct GemmParams {
@@ -188,6 +194,19 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* r) {
   }
 }
 
+// acc[0..1] += (ws * ts[0..1]) * p[0..1], two lanes of fp32 per instruction.
+__device__ __forceinline__ void promote2(float& a0, float& a1, float ws, float t0, float t1, uint32_t p0,
+                                         uint32_t p1) {
+  uint64_t acc, c, ts, w2, pp;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ts) : "f"(t0), "f"(t1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(w2) : "f"(ws));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pp) : "r"(p0), "r"(p1));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(c) : "l"(w2), "l"(ts));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(c), "l"(pp));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc));
+}
+
 template <class CF>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAS,
@@ -195,7 +214,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const GemmParams prm) {
   constexpr int NMAX = CF::NMAX;
   constexpr int STAGES = CF::STAGES;
+  constexpr int SSTAGES = CF::SSTAGES;
   constexpr int ABUF = CF::ABUF;
+  constexpr int NP = CF::NP;
   constexpr int NHALF = NMAX / 2;
 
   extern __shared__ uint8_t smem_raw[];
@@ -203,15 +224,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* s_tok = smem + CF::kOffTok;
   uint8_t* s_wpk = smem + CF::kOffWpk;
   uint8_t* s_a = smem + CF::kOffA;
-  float* s_tsc = reinterpret_cast<float*>(smem + CF::kOffTsc);
-  float* s_wsc = reinterpret_cast<float*>(smem + CF::kOffWsc);
+  uint8_t* s_sc = smem + CF::kOffSc;  // slot: NMAX token scales, then (128-B aligned) 128 weight scales
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + CF::kOffBar);
   uint64_t* full = bars;
-  uint64_t* empty = bars + STAGES;
-  uint64_t* afull = bars + 2 * STAGES;
-  uint64_t* aempty = afull + ABUF;
-  uint64_t* pfull = aempty + ABUF;
-  uint64_t* pempty = pfull + 2;
+  uint64_t* empty = full + STAGES;
+  uint64_t* sfull = empty + STAGES;
+  uint64_t* sempty = sfull + SSTAGES;
+  uint64_t* mready = sempty + SSTAGES;  // [ABUF] converted weights (and their P buffer) ready for the MMA
+  uint64_t* mdone = mready + ABUF;      // [ABUF] MMAs of the group done: A buffer free, partials ready
+  uint64_t* pempty = mdone + ABUF;      // [NP] partial buffer read by the epilogue
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + CF::kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + CF::kOffMisc + 4);
   int* s_prefix = reinterpret_cast<int*>(smem + CF::kOffSched);
@@ -227,20 +248,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConvWarps + 1 + kEpiWarps);
+      mbar_init(&empty[s], kConvWarps + 1);
+    }
+    for (int s = 0; s < SSTAGES; ++s) {
+      mbar_init(&sfull[s], 1);
+      mbar_init(&sempty[s], kEpiWarps);
     }
     for (int b = 0; b < ABUF; ++b) {
-      mbar_init(&afull[b], kConvWarps);
-      mbar_init(&aempty[b], 1);
+      mbar_init(&mready[b], kConvWarps);
+      mbar_init(&mdone[b], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&pfull[b], 1);
-      mbar_init(&pempty[b], kEpiWarps);
-    }
+    for (int b = 0; b < NP; ++b) mbar_init(&pempty[b], kEpiWarps);
     *s_abort = 0;
     mbar_fence_init();
   }
-  if (warp == kWarpMma) {
+  if (warp == kWarpMma) {  // the first MMA warp owns the tensor-memory allocation
     tmem_alloc(s_tmem, CF::kTmemCols);
     tmem_relinquish();
   }
@@ -266,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         s_start[e] = st;
       }
-      int v = (cnt + NMAX - 1) / NMAX;
+      int v = (cnt + CF::kChunkMax - 1) / CF::kChunkMax;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int u = __shfl_up_sync(0xffffffffu, v, o);
@@ -285,45 +307,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   Sched sch{s_prefix, s_start, E, NMAX, nblk};
   const int n_items = s_prefix[E] * nblk;
 
+  // A tile covers rows [row0 & ~3, ...): the scale vectors then start 16-byte aligned.
   if (warp == kWarpTma) {
     if (lane == 0) {
       const uint64_t pol_w = l2_policy_evict_first();
-      const uint32_t bytes = CF::kTokBytes + CF::kTscFloats * 4 + CF::kWpkBytes + kBM * 4;
       uint32_t it = 0;
       for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
         int e, nb, row0, rows;
         sch.decode(item, e, nb, row0, rows);
-        const int x_sc = row0 & ~3;
+        const int r4 = row0 & ~3;
         for (int g = 0; g < G; ++g, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
+          const int ss = it % SSTAGES;
+          const uint32_t sph = (it / SSTAGES) & 1;
           if (!wait_bar(&empty[s], ph ^ 1, s_abort)) goto done;
-          mbar_arrive_expect_tx(&full[s], bytes);
-          tma_load_2d(s_tok + s * CF::kTokBytes, &tmA, &full[s], g * kGroup, row0);
-          tma_load_2d(s_tsc + s * CF::kTscStride, &tmAS, &full[s], x_sc, g);
-          tma_load_2d_hint(s_wpk + s * CF::kWpkBytes, &tmB, &full[s], g * (kGroup / 2),
-                           e * prm.N + nb * kBM, pol_w);
-          tma_load_2d(s_wsc + s * kBM, &tmBS, &full[s], nb * kBM, e * G + g);
+          mbar_arrive_expect_tx(&full[s], CF::kTokBytes + CF::kWpkBytes);
+          tma_load_2d(s_tok + s * CF::kTokBytes, &tmA, &full[s], g * kGroup, r4);
+          tma_load_2d_hint(s_wpk + s * CF::kWpkBytes, &tmB, &full[s], g * (kGroup / 2), e * prm.N + nb * kBM,
+                           pol_w);
+          if (!wait_bar(&sempty[ss], sph ^ 1, s_abort)) goto done;
+          uint8_t* sc = s_sc + ss * CF::kScBytes;
+          mbar_arrive_expect_tx(&sfull[ss], NMAX * 4 + kBM * 4);
+          tma_load_2d(sc, &tmAS, &sfull[ss], r4, g);
+          tma_load_2d(sc + CF::kWscOff, &tmBS, &sfull[ss], nb * kBM, e * G + g);
         }
       }
     }
-  } else if (warp == kWarpMma) {
+  } else if (warp < kWarpConv0) {
+    // ---- MMA issue: one thread per group set ----
+    const int mset = warp - kWarpMma;
     if (lane == 0) {
       uint32_t it = 0;
       for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
         int e, nb, row0, rows;
         sch.decode(item, e, nb, row0, rows);
-        const uint32_t idesc = idesc_e4m3(static_cast<uint32_t>((rows + 15) & ~15));
+        const int ncol = (row0 - (row0 & ~3) + rows + 15) & ~15;
+        const uint32_t idesc = idesc_e4m3(static_cast<uint32_t>(ncol));
         for (int g = 0; g < G; ++g, ++it) {
+          if (static_cast<int>(it % kConvSets) != mset) continue;
           const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
           const int b = it % ABUF;
           const uint32_t aph = (it / ABUF) & 1;
-          const int pb = it & 1;
-          const uint32_t pph = (it >> 1) & 1;
-          if (!wait_bar(&full[s], ph, s_abort)) goto done;
-          if (!wait_bar(&afull[b], aph, s_abort)) goto done;
-          if (!wait_bar(&pempty[pb], pph ^ 1, s_abort)) goto done;
+          const int pb = it % NP;
+          // mready implies: token tile landed, weights converted, partial buffer free
+          if (!wait_bar(&mready[b], aph, s_abort)) goto done;
           tc_fence_after();
           const uint32_t d = tmem_base + pb * NMAX;
           const uint32_t tok = smem_u32(s_tok + s * CF::kTokBytes);
@@ -339,23 +367,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           mma_commit(&empty[s]);
-          mma_commit(&aempty[b]);
-          mma_commit(&pfull[pb]);
+          mma_commit(&mdone[b]);
         }
       }
     }
   } else if (warp < kWarpEpi0) {
-    // ---- converters: int4 -> E4M3 ----
+    // ---- converters: int4 -> E4M3; set `cset` takes every kConvSets-th group ----
     const int q4 = warp & 3;
+    const int cset = (warp - kWarpConv0) / kConvWarps;
     const int r = q4 * 32 + lane;
     uint32_t it = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
       for (int g = 0; g < G; ++g, ++it) {
+        if (static_cast<int>(it % kConvSets) != cset) continue;
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
         const int b = it % ABUF;
         const uint32_t aph = (it / ABUF) & 1;
-        const bool ok = wait_bar(&full[s], ph, s_abort) && wait_bar(&aempty[b], aph ^ 1, s_abort);
+        const int pb = it % NP;
+        const uint32_t pph = (it / NP) & 1;
+        const bool ok = wait_bar(&full[s], ph, s_abort) && wait_bar(&mdone[b], aph ^ 1, s_abort) &&
+                        wait_bar(&pempty[pb], pph ^ 1, s_abort);
         if (__any_sync(0xffffffffu, !ok)) goto done;  // warp-uniform; the warp is converged below
         const uint8_t* wrow = s_wpk + s * CF::kWpkBytes + r * 64;
         uint32_t in[16];
@@ -386,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&afull[b]);
+        if (lane == 0) mbar_arrive(&mready[b]);
       }
     }
   } else {
@@ -396,42 +428,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = q4 * 32 + lane;
     const int c0 = half * NHALF;
     const uint32_t t_lane = static_cast<uint32_t>(q4 * 32) << 16;
+    constexpr int CH = NHALF < 16 ? NHALF : 16;
     uint32_t it = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
       int e, nb, row0, rows;
       sch.decode(item, e, nb, row0, rows);
-      const int sc_off = row0 - (row0 & ~3) + c0;
+      const int r4 = row0 & ~3;
+      const int lo = row0 - r4;  // columns [lo, lo + rows) of the tile are this chunk's rows
       float acc[NHALF];
 #pragma unroll
       for (int j = 0; j < NHALF; ++j) acc[j] = 0.f;
       for (int g = 0; g < G; ++g, ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        const int pb = it & 1;
-        const uint32_t pph = (it >> 1) & 1;
-        const bool ok = wait_bar(&pfull[pb], pph, s_abort) && wait_bar(&full[s], ph, s_abort);
+        const int ss = it % SSTAGES;
+        const uint32_t sph = (it / SSTAGES) & 1;
+        const int pb = it % NP;
+        const int b = it % ABUF;
+        const uint32_t aph = (it / ABUF) & 1;
+        const bool ok = wait_bar(&mdone[b], aph, s_abort) && wait_bar(&sfull[ss], sph, s_abort);
         if (__any_sync(0xffffffffu, !ok)) goto done;  // warp-uniform; tcgen05.ld needs a converged warp
         tc_fence_after();
-        const float ws = s_wsc[s * kBM + r];
-        const float* ts = s_tsc + s * CF::kTscStride + sc_off;
-        constexpr int CH = NHALF < 32 ? NHALF : 32;
+        const float* sc = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes);
+        const float ws = sc[CF::kWscOff / 4 + r];
 #pragma unroll
         for (int c = 0; c < NHALF; c += CH) {
           uint32_t p[CH];
           tmem_load_cols<CH>(tmem_base + t_lane + pb * NMAX + c0 + c, p);
           tmem_wait_ld();
+          if (c + CH >= NHALF) {  // last chunk read: hand the buffer back to the MMA
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pempty[pb]);
+          }
 #pragma unroll
-          for (int j = 0; j < CH; ++j) acc[c + j] = fmaf(ws * ts[c + j], __uint_as_float(p[j]), acc[c + j]);
+          for (int j = 0; j < CH; j += 4) {
+            const float4 t = *reinterpret_cast<const float4*>(sc + c0 + c + j);
+            promote2(acc[c + j], acc[c + j + 1], ws, t.x, t.y, p[j], p[j + 1]);
+            promote2(acc[c + j + 2], acc[c + j + 3], ws, t.z, t.w, p[j + 2], p[j + 3]);
+          }
         }
-        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&pempty[pb]);
-        if (lane == 0) mbar_arrive(&empty[s]);
+        if (lane == 0) mbar_arrive(&sempty[ss]);
       }
-      uint16_t* crow = prm.C + static_cast<int64_t>(row0) * prm.N + nb * kBM + r;
+      uint16_t* crow = prm.C + static_cast<int64_t>(r4) * prm.N + nb * kBM + r;
 #pragma unroll
-      for (int j = 0; j < NHALF; ++j)
-        if (c0 + j < rows) crow[static_cast<int64_t>(c0 + j) * prm.N] = float_to_bf16_bits(acc[j]);
+      for (int j = 0; j < NHALF; ++j) {
+        const int t = c0 + j;
+        if (t >= lo && t < lo + rows) crow[static_cast<int64_t>(t) * prm.N] = float_to_bf16_bits(acc[j]);
+      }
     }
   }
 done:
@@ -502,7 +545,7 @@ int launch(const uint8_t* A, const float* a_s, int64_t a_ld, const uint8_t* B, c
   if ((rc = make_map_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, CF::NMAX,
                         CU_TENSOR_MAP_SWIZZLE_128B, "A")))
     return rc;
-  if ((rc = make_map_2d(&tAS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a_s, a_ld, G, a_ld * 4, CF::kTscFloats, 1,
+  if ((rc = make_map_2d(&tAS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a_s, a_ld, G, a_ld * 4, CF::NMAX, 1,
                         CU_TENSOR_MAP_SWIZZLE_NONE, "a_scales")))
     return rc;
   if ((rc = make_map_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K / 2, E * N, K / 2, 64, kBM,
@@ -529,8 +572,10 @@ int launch(const uint8_t* A, const float* a_s, int64_t a_ld, const uint8_t* B, c
   return check_launch("w4a8_gemm_kernel");
 }
 
-using CfgDecode = Cfg<16, 12, 3, false>;
-using CfgPrefill = Cfg<128, 5, 2, false>;
+// decode: few rows per expert, weight streaming; converted weights in tensor memory
+using CfgDecode = Cfg<16, 16, 24, 8, 8, true>;
+// prefill: 128-row token tiles, four partial buffers fill tensor memory; weights in shared memory
+using CfgPrefill = Cfg<128, 5, 16, 4, 4, false>;
 
 int gemm_common(const uint8_t* A, const float* a_s, int64_t a_ld, const uint8_t* B, const float* b_s,
                 const int64_t* seg, int64_t E, int64_t N, int64_t K, int64_t M, uint16_t* C, void* stream) {
