@@ -182,9 +182,10 @@ class MoeRunner:
         self.cfg = cfg
         T, H, I, E, k = (cfg[x] for x in ("T", "H", "I", "E", "k"))
         self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
-        self.w13 = inputs.gpu_packed_int4(seed, inputs.STREAM_W13, (E, 2 * I, H // 2), dev)
+        # weights are prepacked once after generation (the post-load processing step), untimed
+        self.w13 = m.w4a8_prepack_weights(inputs.gpu_packed_int4(seed, inputs.STREAM_W13, (E, 2 * I, H // 2), dev))
         self.w13s = inputs.gpu_scales(seed, inputs.STREAM_W13_SCALE, (E, H // 128, 2 * I), dev)
-        self.w2 = inputs.gpu_packed_int4(seed, inputs.STREAM_W2, (E, H, I // 2), dev)
+        self.w2 = m.w4a8_prepack_weights(inputs.gpu_packed_int4(seed, inputs.STREAM_W2, (E, H, I // 2), dev))
         self.w2s = inputs.gpu_scales(seed, inputs.STREAM_W2_SCALE, (E, I // 128, H), dev)
         x_bits = inputs.activations_bf16(seed, T, H)
         logits = inputs.router_logits(seed, T, E, cfg.get("zipf"))
@@ -199,7 +200,7 @@ class MoeRunner:
         b = self.ws.data_ptr()
         L = self.L
         self.p = {n: b + getattr(L, n) for n in ("topk_ids", "topk_w", "seg_indptr", "src2dst", "dst2src",
-                                                 "xq", "xs", "y13", "hq", "hs", "y2")}
+                                                 "xq", "xs", "xc", "y13", "hq", "hs", "hc", "y2")}
         self.ld = L.scale_ld
 
     def stages(self, stream):
@@ -212,13 +213,13 @@ class MoeRunner:
             ("route", lambda: lib.moe_route_topk(lg, T, E, k, 1, p["topk_ids"], p["topk_w"], stream)),
             ("permute", lambda: lib.moe_permute(p["topk_ids"], T, k, E, p["seg_indptr"], p["src2dst"],
                                                 p["dst2src"], None, 0, stream)),
-            ("quant", lambda: lib.fp8_quant_per_token_group(x, T, H, p["dst2src"], k, P, p["xq"], p["xs"], ld,
-                                                            stream)),
-            ("w13", lambda: lib.w4a8_grouped_gemm(p["xq"], p["xs"], ld, w13, w13s, p["seg_indptr"], E, 2 * I, H,
-                                                  P, p["y13"], None, 0, stream)),
-            ("silu_requant", lambda: lib.silu_mul_requant(p["y13"], P, I, p["hq"], p["hs"], ld, stream)),
-            ("w2", lambda: lib.w4a8_grouped_gemm(p["hq"], p["hs"], ld, w2, w2s, p["seg_indptr"], E, H, I, P,
-                                                 p["y2"], None, 0, stream)),
+            ("quant", lambda: lib.fp8_quant_per_token_group(x, T, H, p["dst2src"], k, P, p["xq"], p["xs"], p["xc"],
+                                                            ld, stream)),
+            ("w13", lambda: lib.w4a8_grouped_gemm(p["xq"], p["xs"], p["xc"], ld, w13, w13s, p["seg_indptr"], E,
+                                                  2 * I, H, P, p["y13"], None, 0, stream)),
+            ("silu_requant", lambda: lib.silu_mul_requant(p["y13"], P, I, p["hq"], p["hs"], p["hc"], ld, stream)),
+            ("w2", lambda: lib.w4a8_grouped_gemm(p["hq"], p["hs"], p["hc"], ld, w2, w2s, p["seg_indptr"], E, H, I,
+                                                 P, p["y2"], None, 0, stream)),
             ("combine", lambda: lib.moe_unpermute_combine(p["y2"], p["src2dst"], p["topk_w"], T, k, H, out,
                                                           stream)),
         ]
@@ -391,19 +392,20 @@ def run_linear(args, cfg, dev, world, rank, peaks, peak_src):
     G = K // 128
     # several weight copies so that consecutive steps do not hit L2
     copies = max(1, int(np.ceil(2 * 129e6 / (N * K // 2))))
-    Ws = [inputs.gpu_packed_int4(args.seed + c, inputs.STREAM_LIN_W, (N, K // 2), dev) for c in range(copies)]
+    Ws = [m.w4a8_prepack_weights(inputs.gpu_packed_int4(args.seed + c, inputs.STREAM_LIN_W, (N, K // 2), dev))
+          for c in range(copies)]
     Ss = [inputs.gpu_scales(args.seed + c, inputs.STREAM_LIN_SCALE, (G, N), dev) for c in range(copies)]
     rng = np.random.default_rng(args.seed)
     x = torch.from_numpy(inputs.to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32)).view(np.int16)).view(
         torch.bfloat16).to(dev)
-    aq, a_s = m.fp8_quant_per_token_group(x)
+    aq, a_s, a_c = m.fp8_quant_per_token_group(x)
     C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     need = m.linear_workspace_bytes(M, N, K)
     ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     sp = torch.cuda.current_stream(dev).cuda_stream
 
     def step(i):
-        return lib.w4a8_linear(aq.data_ptr(), a_s.data_ptr(), a_s.shape[1], Ws[i % copies].data_ptr(),
+        return lib.w4a8_linear(aq.data_ptr(), a_s.data_ptr(), a_c.data_ptr(), a_s.shape[1], Ws[i % copies].data_ptr(),
                                Ss[i % copies].data_ptr(), M, N, K, C.data_ptr(), ws.data_ptr(), need, sp)
 
     for i in range(args.warmup):

@@ -30,11 +30,17 @@
  * Packed weight layout (canonical): uint8 [E][N][K/2].  Byte b of a row
  * holds element k = 2b in bits 0-3 and k = 2b+1 in bits 4-7, each a two's
  * complement nibble in -8..7 (lower k in lower bits, the unpack order of the
- * SGLang PR #37796 page, Modifications).  Weight scales: fp32 [E][K/128][N]
+ * SGLang PR #37796 page, Modifications).  The GEMMs take weights prepacked once
+ * by w4a8_prepack_weights (same size and row layout, another code per nibble;
+ * the post-load weight processing step of the PR #7762 page,
+ * process_weights_after_loading).  Weight scales: fp32 [E][K/128][N]
  * (N contiguous, the [E, K/128, N] scale layout of the PR #37796 page).
  * Activation scales: fp32 [K/128][ld], element (row m, group g) at
  * scales[g*ld + m], ld >= M and ld % 4 == 0 (group-major, so a tile of rows of
- * one group is contiguous for TMA).
+ * one group is contiguous for TMA).  Activation corrections gcorr: same layout,
+ * gcorr[g][m] = -1/2 * scales[g][m] * sum_{k in g} e4m3(q[m][k]); the
+ * quantisation calls emit them and the GEMMs consume them (the prepacked
+ * weights encode v + 1/2, whose products the correction removes).
  */
 #ifndef W4A8MOE_H
 #define W4A8MOE_H
@@ -46,7 +52,7 @@
 extern "C" {
 #endif
 
-#define W4A8MOE_ABI_VERSION 1
+#define W4A8MOE_ABI_VERSION 2
 
 typedef enum {
   W4A8_OK = 0,
@@ -112,12 +118,12 @@ int moe_permute(const int32_t* topk_ids, int64_t T, int k, int64_t E, int64_t* s
  * row_index = NULL output row j reads input row j and M_out must equal M_src.
  * In the MoE this quantises the permuted copy directly (row_index = dst2src,
  * row_div = k); quantisation is per row, so it equals permuting quantised rows.
- *   x bf16 [M_src][K]   q uint8 [M_out][K]   scales fp32 [K/128][scale_ld]
- *   K % 128 == 0, scale_ld >= M_out, scale_ld % 4 == 0.
+ *   x bf16 [M_src][K]   q uint8 [M_out][K]   scales, gcorr fp32 [K/128][scale_ld]
+ *   K % 128 == 0, scale_ld >= M_out, scale_ld % 4 == 0.  gcorr may be NULL.
  */
 int fp8_quant_per_token_group(const uint16_t* x, int64_t M_src, int64_t K,
                               const int32_t* row_index, int64_t row_div, int64_t M_out,
-                              uint8_t* q, float* scales, int64_t scale_ld, void* stream);
+                              uint8_t* q, float* scales, float* gcorr, int64_t scale_ld, void* stream);
 
 /*
  * (4) Grouped int4 x FP8 GEMM (PR #7762 page: CUTLASS W4A8 grouped GEMM,
@@ -125,17 +131,27 @@ int fp8_quant_per_token_group(const uint16_t* x, int64_t M_src, int64_t K,
  *   C[j][n] = bf16( sum_g a_s[g][j] * b_s[e][g][n] *
  *                   sum_{k in group g} e4m3(A[j][k]) * int4(B[e][n][k]) )
  * accumulated in fp32 per group on the tensor cores and promoted in fp32.
- *   A uint8 [M_total][K] (E4M3 codes)         a_scales fp32 [K/128][a_scale_ld]
- *   B_packed uint8 [E][N][K/2] (canonical)    b_scales fp32 [E][K/128][N]
+ *   A uint8 [M_total][K] (E4M3 codes)   a_scales, a_gcorr fp32 [K/128][a_scale_ld]
+ *   B_prepacked uint8 [E][N][K/2] (w4a8_prepack_weights)   b_scales fp32 [E][K/128][N]
  *   seg_indptr int64 [E+1] (device; seg_indptr[E] must equal M_total)
  *   C bf16 [M_total][N]
  *   K % 128 == 0, N % 128 == 0, 1 <= E <= 1024, M_total < 2^31.
  * Rows outside every segment are not written.  ws may be NULL (none needed).
  */
-int w4a8_grouped_gemm(const uint8_t* A, const float* a_scales, int64_t a_scale_ld,
-                      const uint8_t* B_packed, const float* b_scales, const int64_t* seg_indptr,
-                      int64_t E, int64_t N, int64_t K, int64_t M_total, uint16_t* C, void* ws,
-                      size_t ws_bytes, void* stream);
+int w4a8_grouped_gemm(const uint8_t* A, const float* a_scales, const float* a_gcorr,
+                      int64_t a_scale_ld, const uint8_t* B_prepacked, const float* b_scales,
+                      const int64_t* seg_indptr, int64_t E, int64_t N, int64_t K, int64_t M_total,
+                      uint16_t* C, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * One-time weight re-layout for the GEMMs (the post-load weight processing of
+ * the PR #7762 page, process_weights_after_loading).  Canonical packed int4
+ * rows [rows][K/2] -> prepacked rows of the same shape: within each 32-bit
+ * word of 8 weights, nibble p holds in bits 0-2 the index m with |v + 1/2| =
+ * m + 1/2 and in bit 3 the sign of v of element 4 + p/2 (p even) or (p-1)/2
+ * (p odd).  w and out must not overlap.  K % 8 == 0 (K % 128 for the GEMMs).
+ */
+int w4a8_prepack_weights(const uint8_t* w, int64_t rows, int64_t K, uint8_t* out, void* stream);
 
 /*
  * (5) SiLU and Mul with FP8 re-quantisation of the intermediate (PR #7762
@@ -143,11 +159,11 @@ int w4a8_grouped_gemm(const uint8_t* A, const float* a_scales, int64_t a_scale_l
  * intermediate values).  gate_up row m holds gate in columns [0, I) and up in
  * [I, 2I); h = silu(gate) * up = gate / (1 + exp(-gate)) * up in fp32, then
  * the quantisation of (3) on h.
- *   gate_up bf16 [M][2I]   q uint8 [M][I]   scales fp32 [I/128][scale_ld]
- *   I % 128 == 0, scale_ld >= M, scale_ld % 4 == 0.
+ *   gate_up bf16 [M][2I]   q uint8 [M][I]   scales, gcorr fp32 [I/128][scale_ld]
+ *   I % 128 == 0, scale_ld >= M, scale_ld % 4 == 0.  gcorr may be NULL.
  */
 int silu_mul_requant(const uint16_t* gate_up, int64_t M, int64_t I, uint8_t* q, float* scales,
-                     int64_t scale_ld, void* stream);
+                     float* gcorr, int64_t scale_ld, void* stream);
 
 /*
  * (6) Unpermute and combine (PR #7762 page: post-reordering of the outputs):
@@ -162,14 +178,14 @@ int moe_unpermute_combine(const uint16_t* Y, const int32_t* src2dst, const float
 /*
  * (7) Dense W4AFP8 Linear: (4) with one weight matrix and no routing
  * (lyraW4AFp8 page: Machete mixed-input GEMM for the Linear layers).
- *   A uint8 [M][K]   a_scales fp32 [K/128][a_scale_ld]
- *   B_packed uint8 [N][K/2]   b_scales fp32 [K/128][N]   C bf16 [M][N]
+ *   A uint8 [M][K]   a_scales, a_gcorr fp32 [K/128][a_scale_ld]
+ *   B_prepacked uint8 [N][K/2]   b_scales fp32 [K/128][N]   C bf16 [M][N]
  *   K % 128 == 0, N % 128 == 0.
  * ws: at least w4a8_workspace_bytes(W4A8_OP_LINEAR, M, N, K, 1) bytes (the
  * split-K partial sums of small-M shapes); may be NULL when that is 0.
  */
-int w4a8_linear(const uint8_t* A, const float* a_scales, int64_t a_scale_ld,
-                const uint8_t* B_packed, const float* b_scales, int64_t M, int64_t N, int64_t K,
+int w4a8_linear(const uint8_t* A, const float* a_scales, const float* a_gcorr, int64_t a_scale_ld,
+                const uint8_t* B_prepacked, const float* b_scales, int64_t M, int64_t N, int64_t K,
                 uint16_t* C, void* ws, size_t ws_bytes, void* stream);
 
 /* Operation ids for w4a8_workspace_bytes. */
@@ -185,8 +201,8 @@ size_t w4a8_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int64_t E);
  * permuted hidden states -> (4) w13 -> (5) SiLU and Mul + requantise -> (4) w2
  * -> (6) combine.  Seven launches (plus the permutation's), nothing else.
  *   x bf16 [T][H]   logits fp32 [T][E]
- *   w13 uint8 [E][2I][H/2] (rows [0, I) gate, [I, 2I) up)   w13_s fp32 [E][H/128][2I]
- *   w2 uint8 [E][H][I/2]   w2_s fp32 [E][I/128][H]          out bf16 [T][H]
+ *   w13 uint8 [E][2I][H/2] prepacked (rows [0, I) gate, [I, 2I) up)   w13_s fp32 [E][H/128][2I]
+ *   w2 uint8 [E][H][I/2] prepacked   w2_s fp32 [E][I/128][H]          out bf16 [T][H]
  *   ws: w4a8_moe_workspace_bytes(T, H, I, E, k) bytes, 256-byte aligned; it
  *   holds the intermediates (ids, weights, permutation, FP8 codes and scales,
  *   Y13, Y2), whose offsets are given by w4a8_moe_workspace_layout.
@@ -222,7 +238,7 @@ size_t w4a8_moe_noalloc_scratch_bytes(void);
 
 /* Byte offsets of the intermediates inside the w4a8_moe_forward workspace. */
 typedef struct {
-  size_t topk_ids, topk_w, seg_indptr, src2dst, dst2src, xq, xs, y13, hq, hs, y2, permute_ws;
+  size_t topk_ids, topk_w, seg_indptr, src2dst, dst2src, xq, xs, xc, y13, hq, hs, hc, y2, permute_ws;
   int64_t scale_ld; /* leading dimension of xs and hs: T*k rounded up to 4 */
   size_t total;
 } w4a8_moe_layout;

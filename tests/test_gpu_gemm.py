@@ -11,7 +11,7 @@ import torch
 import inputs
 import oracle
 from oracle import e4m3
-from gpu_util import f64_of_bf16, rel_fro, scales_to_gpu_layout, to_dev
+from gpu_util import f64_of_bf16, gcorr_of, prepacked, rel_fro, scales_to_gpu_layout, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -28,9 +28,8 @@ def _weights(rng, E, N, K):
 
 
 def _run_grouped(lib, aq, a_s, packed, ws, seg):
-    E, N, _ = packed.shape
-    return lib.w4a8_grouped_gemm(to_dev(aq), scales_to_gpu_layout(a_s), to_dev(packed), to_dev(ws),
-                                 to_dev(seg.astype(np.int64)))
+    return lib.w4a8_grouped_gemm(to_dev(aq), scales_to_gpu_layout(a_s), scales_to_gpu_layout(gcorr_of(aq, a_s)),
+                                 prepacked(lib, packed), to_dev(ws), to_dev(seg.astype(np.int64)))
 
 
 def _oracle_grouped(aq, a_s, packed, ws, seg):
@@ -98,7 +97,8 @@ def test_linear(lib, M, N, K):
     rng = np.random.default_rng(M * 7 + N + K)
     aq, a_s = _acts(rng, M, K)
     packed, ws = _weights(rng, 1, N, K)
-    got = f64_of_bf16(lib.w4a8_linear(to_dev(aq), scales_to_gpu_layout(a_s), to_dev(packed[0]), to_dev(ws[0])))
+    got = f64_of_bf16(lib.w4a8_linear(to_dev(aq), scales_to_gpu_layout(a_s), scales_to_gpu_layout(gcorr_of(aq, a_s)),
+                                      prepacked(lib, packed[0]), to_dev(ws[0])))
     ref = oracle.linear(aq, a_s, oracle.unpack_int4(packed[0]), ws[0].T)
     err = rel_fro(got, ref)
     assert err <= 1e-3, (err, np.abs(got - ref).max())

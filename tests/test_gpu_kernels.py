@@ -11,7 +11,7 @@ import torch
 
 import inputs
 import oracle
-from gpu_util import (bf16_from_bits, bf16_ulp_diff, bits_of_bf16, f64_of_bf16, rel_fro,
+from gpu_util import (bf16_from_bits, bf16_ulp_diff, bits_of_bf16, decode_prepacked, f64_of_bf16, rel_fro,
                       scales_from_gpu_layout, to_dev)
 
 pytestmark = pytest.mark.gpu
@@ -91,10 +91,20 @@ def _bf16_rows(rng, M, K):
 def test_quant(lib, M, K):
     rng = np.random.default_rng(M + K)
     xb = _bf16_rows(rng, M, K)
-    q, s = lib.fp8_quant_per_token_group(bf16_from_bits(xb))
+    q, s, c = lib.fp8_quant_per_token_group(bf16_from_bits(xb))
     rq, rs = oracle.quant_per_token_group(inputs.bf16_bits_to_f32(xb))
     assert np.array_equal(q.cpu().numpy(), rq)
     assert np.array_equal(scales_from_gpu_layout(s, M), rs)
+    _check_gcorr(scales_from_gpu_layout(c, M), rq, rs)
+
+
+def _check_gcorr(gc, codes, scales):
+    # -1/2 * scale * (sum of the group's E4M3 values): the sum is exact in float64
+    M, K = codes.shape
+    S = oracle.e4m3.decode(codes).reshape(M, K // 128, 128).sum(axis=2)
+    ref = -0.5 * scales.astype(np.float64) * S
+    tol = 1e-6 * (0.5 * scales.astype(np.float64) * np.abs(oracle.e4m3.decode(codes)).reshape(M, K // 128, 128).sum(2))
+    assert np.all(np.abs(gc - ref) <= tol + 1e-30)
 
 
 def test_quant_gather(lib):
@@ -103,7 +113,7 @@ def test_quant_gather(lib):
     xb = _bf16_rows(rng, T, K)
     ids = _distinct_ids(rng, T, 16, k)
     _, _, d2s = oracle.permute(ids, 16)
-    q, s = lib.fp8_quant_per_token_group(bf16_from_bits(xb), to_dev(d2s.astype(np.int32)), k)
+    q, s, c = lib.fp8_quant_per_token_group(bf16_from_bits(xb), to_dev(d2s.astype(np.int32)), k)
     rq, rs = oracle.quant_per_token_group(inputs.bf16_bits_to_f32(xb))
     tok = d2s // k
     assert np.array_equal(q.cpu().numpy(), rq[tok])
@@ -120,7 +130,7 @@ def test_silu_mul_requant(lib, M, I):
     if M > 1:
         gu[1, :I] = -200.0                      # silu(-200) ~ 0
     gub = inputs.to_bf16_bits(gu)
-    q, s = lib.silu_mul_requant(bf16_from_bits(gub))
+    q, s, c = lib.silu_mul_requant(bf16_from_bits(gub))
     rq, rs = oracle.silu_mul_requant(inputs.bf16_bits_to_f32(gub).astype(np.float64))
     gq = q.cpu().numpy()
     gs = scales_from_gpu_layout(s, M)
@@ -131,6 +141,7 @@ def test_silu_mul_requant(lib, M, I):
         step = np.abs(gq[diff].astype(np.int32) - rq[diff].astype(np.int32))
         assert np.all((step == 1) | ((gq[diff] & 0x7F) == 0) & ((rq[diff] & 0x7F) <= 1))
     assert rel_fro(oracle.dequant(gq, gs), oracle.dequant(rq, rs)) <= 1e-3
+    _check_gcorr(scales_from_gpu_layout(c, M), gq, gs)
 
 
 @pytest.mark.parametrize("T,k,H", [(1, 1, 8), (64, 8, 7168), (300, 2, 256), (129, 32, 64)])
@@ -148,3 +159,13 @@ def test_combine(lib, T, k, H):
     ulp = bf16_ulp_diff(gb, rb)
     assert ulp.max() <= 1 and (ulp > 0).mean() <= 1e-2
     assert rel_fro(f64_of_bf16(out), ref) <= 1e-3
+
+
+@pytest.mark.parametrize("rows,K", [(1, 8), (3, 256), (4096, 7168)])
+def test_prepack_weights(lib, rows, K):
+    # the prepacked bytes, read with the documented format, hold the same int4 values
+    rng = np.random.default_rng(rows + K)
+    packed = rng.integers(0, 256, size=(rows, K // 2), dtype=np.uint8)
+    packed[0, :4] = [0x00, 0x88, 0x7F, 0xF8]
+    got = lib.w4a8_prepack_weights(to_dev(packed)).cpu().numpy()
+    assert np.array_equal(decode_prepacked(got), oracle.unpack_int4(packed))

@@ -12,17 +12,17 @@ import torch
 
 import inputs
 import oracle
-from gpu_util import bf16_from_bits, bits_of_bf16, f64_of_bf16, rel_fro, to_dev
+from gpu_util import bf16_from_bits, bits_of_bf16, f64_of_bf16, gcorr_of, rel_fro, to_dev
 from helpers import moe_experts, moe_host_inputs
 
 pytestmark = pytest.mark.gpu
 
 
-def _device_weights(seed, cfg):
+def _device_weights(lib, seed, cfg):
     H, I, E = cfg["H"], cfg["I"], cfg["E"]
-    return (inputs.gpu_packed_int4(seed, inputs.STREAM_W13, (E, 2 * I, H // 2)),
+    return (lib.w4a8_prepack_weights(inputs.gpu_packed_int4(seed, inputs.STREAM_W13, (E, 2 * I, H // 2))),
             inputs.gpu_scales(seed, inputs.STREAM_W13_SCALE, (E, H // 128, 2 * I)),
-            inputs.gpu_packed_int4(seed, inputs.STREAM_W2, (E, H, I // 2)),
+            lib.w4a8_prepack_weights(inputs.gpu_packed_int4(seed, inputs.STREAM_W2, (E, H, I // 2))),
             inputs.gpu_scales(seed, inputs.STREAM_W2_SCALE, (E, I // 128, H)))
 
 
@@ -30,7 +30,7 @@ def _run_layer(lib, seed, cfg, x_bits=None, logits=None):
     if x_bits is None:
         x_bits, logits = moe_host_inputs(seed, cfg)
     T, H, I, E, k = (cfg[n] for n in ("T", "H", "I", "E", "k"))
-    w13, w13s, w2, w2s = _device_weights(seed, cfg)
+    w13, w13s, w2, w2s = _device_weights(lib, seed, cfg)
     L = lib.moe_workspace_layout(T, H, I, E, k)
     ws = torch.zeros(L.total, dtype=torch.uint8, device="cuda")
     out = lib.w4a8_moe_forward(bf16_from_bits(x_bits), to_dev(logits), k, w13, w13s, w2, w2s, ws=ws)
@@ -76,9 +76,11 @@ def test_layer_stage_by_stage(lib, name, cfg):
     # (3) quantised permuted activations: exact
     xq = _ws_view(ws, L.xq, torch.uint8, (P, H)).numpy()
     xs = _ws_view(ws, L.xs, torch.float32, (H // 128, ld)).numpy()[:, :P].T
+    xc = _ws_view(ws, L.xc, torch.float32, (H // 128, ld)).numpy()[:, :P].T
     rq, rs = oracle.quant_per_token_group(x)
     tok = rd2s // k
     assert np.array_equal(xq, rq[tok]) and np.array_equal(xs, rs[tok])
+    assert np.allclose(xc, gcorr_of(xq, xs), rtol=1e-5, atol=1e-30)
     # (4) w13 on the device's own inputs (identical to the oracle's): 1e-3
     y13 = _ws_view(ws, L.y13, torch.bfloat16, (P, 2 * I)).float().numpy().astype(np.float64)
     ry13 = oracle.round_bf16(oracle.grouped_gemm(xq, xs, seg, w13h.w, w13h.s))
@@ -86,6 +88,8 @@ def test_layer_stage_by_stage(lib, name, cfg):
     # (5) SiLU-and-Mul requant of the device's Y13
     hq = _ws_view(ws, L.hq, torch.uint8, (P, I)).numpy()
     hs = _ws_view(ws, L.hs, torch.float32, (I // 128, ld)).numpy()[:, :P].T
+    hc = _ws_view(ws, L.hc, torch.float32, (I // 128, ld)).numpy()[:, :P].T
+    assert np.allclose(hc, gcorr_of(hq, hs), rtol=1e-5, atol=1e-30)
     rhq, rhs = oracle.silu_mul_requant(y13)
     assert (hq != rhq).mean() <= 1e-3
     assert rel_fro(oracle.dequant(hq, hs), oracle.dequant(rhq, rhs)) <= 1e-3

@@ -22,11 +22,11 @@ pytestmark = pytest.mark.gpu
 CFGS = [dict(T=64, H=256, I=512, E=8, k=2), dict(T=24, H=1024, I=768, E=16, k=4)]
 
 
-def _weights(seed, cfg):
+def _weights(lib, seed, cfg):
     H, I, E = cfg["H"], cfg["I"], cfg["E"]
-    return (inputs.gpu_packed_int4(seed, inputs.STREAM_W13, (E, 2 * I, H // 2)),
+    return (lib.w4a8_prepack_weights(inputs.gpu_packed_int4(seed, inputs.STREAM_W13, (E, 2 * I, H // 2))),
             inputs.gpu_scales(seed, inputs.STREAM_W13_SCALE, (E, H // 128, 2 * I)),
-            inputs.gpu_packed_int4(seed, inputs.STREAM_W2, (E, H, I // 2)),
+            lib.w4a8_prepack_weights(inputs.gpu_packed_int4(seed, inputs.STREAM_W2, (E, H, I // 2))),
             inputs.gpu_scales(seed, inputs.STREAM_W2_SCALE, (E, I // 128, H)))
 
 
@@ -43,7 +43,7 @@ def test_noalloc_matches_workspace_entry_point(lib):
     for seed, cfg in enumerate(CFGS):
         x_bits, logits = moe_host_inputs(seed, cfg)
         x, lg = bf16_from_bits(x_bits), to_dev(logits)
-        w = _weights(seed, cfg)
+        w = _weights(lib, seed, cfg)
         ref = f64_of_bf16(lib.w4a8_moe_forward(x, lg, cfg["k"], *w))
         for call in range(2):  # the shared array keeps the previous call's contents
             out = torch.full((cfg["T"], cfg["H"]), float("nan"), dtype=torch.bfloat16, device="cuda")

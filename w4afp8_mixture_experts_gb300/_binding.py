@@ -26,13 +26,14 @@ _SIGS = {
     "w4a8_device_error": (_c_int, []),
     "moe_route_topk": (_c_int, [_c_vp, _c_i64, _c_i64, _c_int, _c_int, _c_vp, _c_vp, _c_vp]),
     "moe_permute": (_c_int, [_c_vp, _c_i64, _c_int, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]),
-    "fp8_quant_per_token_group": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_i64, _c_i64, _c_vp, _c_vp,
+    "fp8_quant_per_token_group": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp,
                                            _c_i64, _c_vp]),
-    "w4a8_grouped_gemm": (_c_int, [_c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64,
+    "w4a8_grouped_gemm": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64,
                                    _c_i64, _c_vp, _c_vp, _c_sz, _c_vp]),
-    "silu_mul_requant": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp]),
+    "w4a8_prepack_weights": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_vp]),
+    "silu_mul_requant": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64, _c_vp]),
     "moe_unpermute_combine": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_int, _c_i64, _c_vp, _c_vp]),
-    "w4a8_linear": (_c_int, [_c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp,
+    "w4a8_linear": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp,
                              _c_sz, _c_vp]),
     "w4a8_workspace_bytes": (_c_sz, [_c_int, _c_i64, _c_i64, _c_i64, _c_i64]),
     "w4a8_moe_forward": (_c_int, [_c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_vp,
@@ -46,7 +47,8 @@ _SIGS = {
 
 class MoeLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("topk_ids", "topk_w", "seg_indptr", "src2dst", "dst2src",
-                                               "xq", "xs", "y13", "hq", "hs", "y2", "permute_ws")] + \
+                                               "xq", "xs", "xc", "y13", "hq", "hs", "hc", "y2",
+                                               "permute_ws")] + \
                [("scale_ld", ctypes.c_int64), ("total", ctypes.c_size_t)]
 
 
@@ -131,7 +133,7 @@ def moe_permute(topk_ids, E: int):
 
 
 def fp8_quant_per_token_group(x, row_index=None, row_div: int = 1, m_out: int | None = None):
-    """bf16 [M, K] -> (E4M3 codes uint8 [M_out, K], scales fp32 [K/128, ld])."""
+    """bf16 [M, K] -> (E4M3 codes uint8 [M_out, K], scales fp32 [K/128, ld], gcorr fp32 [K/128, ld])."""
     _req(x, torch.bfloat16, "x", 2)
     M, K = x.shape
     if row_index is not None:
@@ -140,27 +142,40 @@ def fp8_quant_per_token_group(x, row_index=None, row_div: int = 1, m_out: int | 
     else:
         m_out = M
     ld = scale_ld(m_out)
+    G = K // 128 if K % 128 == 0 else 1
     q = torch.empty((m_out, K), dtype=torch.uint8, device=x.device)
-    s = torch.empty((K // 128 if K % 128 == 0 else 1, ld), dtype=torch.float32, device=x.device)
-    _check(load().fp8_quant_per_token_group(_p(x), M, K, _p(row_index), row_div, m_out, _p(q), _p(s), ld,
+    s = torch.empty((G, ld), dtype=torch.float32, device=x.device)
+    c = torch.empty((G, ld), dtype=torch.float32, device=x.device)
+    _check(load().fp8_quant_per_token_group(_p(x), M, K, _p(row_index), row_div, m_out, _p(q), _p(s), _p(c), ld,
                                             _stream()))
-    return q, s
+    return q, s, c
 
 
-def w4a8_grouped_gemm(A, a_scales, B_packed, b_scales, seg_indptr):
-    """A uint8 [M, K], a_scales [K/128, ld], B uint8 [E, N, K/2], b_scales [E, K/128, N] -> bf16 [M, N]."""
+def w4a8_prepack_weights(w):
+    """Canonical packed int4 uint8 [..., K/2] -> the GEMMs' prepacked layout (same shape)."""
+    _req(w, torch.uint8, "w")
+    out = torch.empty_like(w)
+    K = w.shape[-1] * 2
+    _check(load().w4a8_prepack_weights(_p(w), w.numel() // (K // 2), K, _p(out), _stream()))
+    return out
+
+
+def w4a8_grouped_gemm(A, a_scales, a_gcorr, B_prepacked, b_scales, seg_indptr):
+    """A uint8 [M, K], a_scales / a_gcorr [K/128, ld], B prepacked uint8 [E, N, K/2],
+    b_scales [E, K/128, N] -> bf16 [M, N]."""
     _req(A, torch.uint8, "A", 2)
     _req(a_scales, torch.float32, "a_scales", 2)
-    _req(B_packed, torch.uint8, "B_packed", 3)
+    _req(a_gcorr, torch.float32, "a_gcorr", 2)
+    _req(B_prepacked, torch.uint8, "B_prepacked", 3)
     _req(b_scales, torch.float32, "b_scales", 3)
     _req(seg_indptr, torch.int64, "seg_indptr", 1)
     M, K = A.shape
-    E, N, Kh = B_packed.shape
-    if Kh * 2 != K or seg_indptr.numel() != E + 1:
+    E, N, Kh = B_prepacked.shape
+    if Kh * 2 != K or seg_indptr.numel() != E + 1 or a_gcorr.shape != a_scales.shape:
         raise ValueError("shape mismatch")
     C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
-    _check(load().w4a8_grouped_gemm(_p(A), _p(a_scales), a_scales.shape[1], _p(B_packed), _p(b_scales),
-                                    _p(seg_indptr), E, N, K, M, _p(C), None, 0, _stream()))
+    _check(load().w4a8_grouped_gemm(_p(A), _p(a_scales), _p(a_gcorr), a_scales.shape[1], _p(B_prepacked),
+                                    _p(b_scales), _p(seg_indptr), E, N, K, M, _p(C), None, 0, _stream()))
     return C
 
 
@@ -171,8 +186,9 @@ def silu_mul_requant(gate_up):
     ld = scale_ld(M)
     q = torch.empty((M, I), dtype=torch.uint8, device=gate_up.device)
     s = torch.empty((max(1, I // 128), ld), dtype=torch.float32, device=gate_up.device)
-    _check(load().silu_mul_requant(_p(gate_up), M, I, _p(q), _p(s), ld, _stream()))
-    return q, s
+    c = torch.empty((max(1, I // 128), ld), dtype=torch.float32, device=gate_up.device)
+    _check(load().silu_mul_requant(_p(gate_up), M, I, _p(q), _p(s), _p(c), ld, _stream()))
+    return q, s, c
 
 
 def moe_unpermute_combine(Y, src2dst, topk_w):
@@ -190,20 +206,22 @@ def linear_workspace_bytes(M: int, N: int, K: int) -> int:
     return int(load().w4a8_workspace_bytes(3, M, N, K, 1))
 
 
-def w4a8_linear(A, a_scales, B_packed, b_scales, ws=None):
-    """A uint8 [M, K], a_scales [K/128, ld], B uint8 [N, K/2], b_scales [K/128, N] -> bf16 [M, N]."""
+def w4a8_linear(A, a_scales, a_gcorr, B_prepacked, b_scales, ws=None):
+    """A uint8 [M, K], a_scales / a_gcorr [K/128, ld], B prepacked uint8 [N, K/2], b_scales [K/128, N]
+    -> bf16 [M, N]."""
     _req(A, torch.uint8, "A", 2)
     _req(a_scales, torch.float32, "a_scales", 2)
-    _req(B_packed, torch.uint8, "B_packed", 2)
+    _req(a_gcorr, torch.float32, "a_gcorr", 2)
+    _req(B_prepacked, torch.uint8, "B_prepacked", 2)
     _req(b_scales, torch.float32, "b_scales", 2)
     M, K = A.shape
-    N = B_packed.shape[0]
+    N = B_prepacked.shape[0]
     need = linear_workspace_bytes(M, N, K)
     if need and ws is None:
         ws = torch.empty(need, dtype=torch.uint8, device=A.device)
     C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
-    _check(load().w4a8_linear(_p(A), _p(a_scales), a_scales.shape[1], _p(B_packed), _p(b_scales), M, N, K,
-                              _p(C), _p(ws), 0 if ws is None else ws.numel(), _stream()))
+    _check(load().w4a8_linear(_p(A), _p(a_scales), _p(a_gcorr), a_scales.shape[1], _p(B_prepacked), _p(b_scales),
+                              M, N, K, _p(C), _p(ws), 0 if ws is None else ws.numel(), _stream()))
     return C
 
 
@@ -214,8 +232,8 @@ def moe_workspace_layout(T: int, H: int, I: int, E: int, k: int) -> MoeLayout:
 
 
 def w4a8_moe_forward(x, logits, k: int, w13, w13_s, w2, w2_s, renormalize: bool = True, ws=None, out=None):
-    """The whole layer.  x bf16 [T, H], logits fp32 [T, E], w13 uint8 [E, 2I, H/2],
-    w13_s fp32 [E, H/128, 2I], w2 uint8 [E, H, I/2], w2_s fp32 [E, I/128, H] -> bf16 [T, H]."""
+    """The whole layer.  x bf16 [T, H], logits fp32 [T, E], w13 prepacked uint8 [E, 2I, H/2],
+    w13_s fp32 [E, H/128, 2I], w2 prepacked uint8 [E, H, I/2], w2_s fp32 [E, I/128, H] -> bf16 [T, H]."""
     _req(x, torch.bfloat16, "x", 2)
     _req(logits, torch.float32, "logits", 2)
     _req(w13, torch.uint8, "w13", 3)

@@ -69,9 +69,11 @@ int layout_of(int64_t T, int64_t H, int64_t I, int64_t E, int k, w4a8_moe_layout
   L->dst2src = take(P * 4);
   L->xq = take(P * H);
   L->xs = take((H / 128) * ld * 4);
+  L->xc = take((H / 128) * ld * 4);
   L->y13 = take(P * 2 * I * 2);
   L->hq = take(P * I);
   L->hs = take((I / 128) * ld * 4);
+  L->hc = take((I / 128) * ld * 4);
   L->y2 = take(P * H * 2);
   L->permute_ws = take(0);
   L->scale_ld = ld;
@@ -144,17 +146,20 @@ extern "C" int w4a8_moe_forward(const uint16_t* x, const float* logits, int64_t 
   int32_t* d2s = reinterpret_cast<int32_t*>(b + L.dst2src);
   uint8_t* xq = b + L.xq;
   float* xs = reinterpret_cast<float*>(b + L.xs);
+  float* xc = reinterpret_cast<float*>(b + L.xc);
   uint16_t* y13 = reinterpret_cast<uint16_t*>(b + L.y13);
   uint8_t* hq = b + L.hq;
   float* hs = reinterpret_cast<float*>(b + L.hs);
+  float* hc = reinterpret_cast<float*>(b + L.hc);
   uint16_t* y2 = reinterpret_cast<uint16_t*>(b + L.y2);
   const int64_t P = T * k;
   if ((rc = moe_route_topk(logits, T, E, k, renormalize, ids, tw, stream))) return rc;
   if ((rc = moe_permute(ids, T, k, E, seg, s2d, d2s, nullptr, 0, stream))) return rc;
-  if ((rc = fp8_quant_per_token_group(x, T, H, d2s, k, P, xq, xs, L.scale_ld, stream))) return rc;
-  if ((rc = w4a8_grouped_gemm(xq, xs, L.scale_ld, w13, w13_s, seg, E, 2 * I, H, P, y13, nullptr, 0, stream)))
+  if ((rc = fp8_quant_per_token_group(x, T, H, d2s, k, P, xq, xs, xc, L.scale_ld, stream))) return rc;
+  if ((rc = w4a8_grouped_gemm(xq, xs, xc, L.scale_ld, w13, w13_s, seg, E, 2 * I, H, P, y13, nullptr, 0, stream)))
     return rc;
-  if ((rc = silu_mul_requant(y13, P, I, hq, hs, L.scale_ld, stream))) return rc;
-  if ((rc = w4a8_grouped_gemm(hq, hs, L.scale_ld, w2, w2_s, seg, E, H, I, P, y2, nullptr, 0, stream))) return rc;
+  if ((rc = silu_mul_requant(y13, P, I, hq, hs, hc, L.scale_ld, stream))) return rc;
+  if ((rc = w4a8_grouped_gemm(hq, hs, hc, L.scale_ld, w2, w2_s, seg, E, H, I, P, y2, nullptr, 0, stream)))
+    return rc;
   return moe_unpermute_combine(y2, s2d, tw, T, k, H, out, stream);
 }

@@ -46,14 +46,8 @@ namespace {
 constexpr int kBM = 128;      // weight rows per tile (MMA M)
 constexpr int kKStep = 32;    // K per tcgen05.mma for 8-bit operands
 constexpr int kWarpTma = 0;
-constexpr int kConvSets = 2;                 // group sets: set c takes the groups with it % 2 == c
 constexpr int kWarpMma = 1;                  // warps 1 .. kConvSets issue the MMAs of one set each
-constexpr int kWarpConv0 = kWarpMma + kConvSets;
 constexpr int kConvWarps = 4;                // converter warps per set: one per tensor-memory lane quarter
-constexpr int kWarpEpi0 = kWarpConv0 + kConvSets * kConvWarps;
-constexpr int kEpiWarps = 8;
-constexpr int kWarps = kWarpEpi0 + kEpiWarps;
-constexpr int kThreads = kWarps * 32;
 constexpr int kMaxExperts = 1024;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s: no legitimate wait comes close
 
@@ -65,22 +59,30 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
   return p;
 }
 
-template <int NMAX_, int STAGES_, int SSTAGES_, int ABUF_, int NP_, bool A_TMEM_>
+template <int NMAX_, int GPS_, int STAGES_, int SSTAGES_, int ABUF_, int NP_, bool A_TMEM_, int SETS_, int EPIW_>
 struct Cfg {
+  // warp roles: 0 TMA producer | 1..SETS MMA issue | SETS x 4 converters | EPIW epilogue
+  static constexpr int kConvSets = SETS_;   // group sets: set c takes the groups with it % SETS == c
+  static constexpr int kEpiWarps = EPIW_;   // 4 or 8 (one or two per tensor-memory lane quarter)
+  static constexpr int kWarpConv0 = kWarpMma + kConvSets;
+  static constexpr int kWarpEpi0 = kWarpConv0 + kConvSets * kConvWarps;
+  static constexpr int kWarps = kWarpEpi0 + kEpiWarps;
+  static constexpr int kThreads = kWarps * 32;
   static constexpr int NMAX = NMAX_;        // token tile (MMA N upper bound)
-  static constexpr int STAGES = STAGES_;    // main ring: token tile + packed weights
-  static constexpr int SSTAGES = SSTAGES_;  // scale ring: token + weight scales (epilogue only)
-  static constexpr int ABUF = ABUF_;        // converted weight buffers
+  static constexpr int GPS = GPS_;          // most 128-K groups per pipeline stage
+  static constexpr int STAGES = STAGES_;    // main ring: token tiles + packed weights of GPS groups
+  static constexpr int SSTAGES = SSTAGES_;  // scale ring: token + weight scales of GPS groups (epilogue)
+  static constexpr int ABUF = ABUF_;        // converted weight buffers (one group each)
   static constexpr int NP = NP_;            // fp32 partial-product buffers in tensor memory
   static constexpr bool A_TMEM = A_TMEM_;   // converted weights in tensor memory (else shared)
-  static constexpr int kTokBytes = NMAX * 128;            // NMAX rows x 128 B, 128B swizzle
-  static constexpr int kWpkBytes = kBM * 64;              // 128 rows x 64 B packed int4
+  static constexpr int kTokBytes = NMAX * 128;            // one group: NMAX rows x 128 B, 128B swizzle
+  static constexpr int kWpkBytes = kBM * 64;              // one group: 128 rows x 64 B packed int4
   static constexpr int kABytes = kBM * 128;               // 128 rows x 128 B E4M3
-  static constexpr int kWscOff = (NMAX * 4 + 127) / 128 * 128;          // weight scales in a slot
-  static constexpr int kScBytes = kWscOff + kBM * 4;                      // one scale slot (128-B aligned)
+  static constexpr int kTscBytes = (GPS * NMAX * 4 + 127) / 128 * 128;  // token scales (and corrections) of a slot
+  static constexpr int kScBytes = 2 * kTscBytes + GPS * kBM * 4;        // one scale slot
   static constexpr int kOffTok = 0;
-  static constexpr int kOffWpk = kOffTok + STAGES * kTokBytes;
-  static constexpr int kOffA = kOffWpk + STAGES * kWpkBytes;
+  static constexpr int kOffWpk = kOffTok + STAGES * GPS * kTokBytes;
+  static constexpr int kOffA = kOffWpk + STAGES * GPS * kWpkBytes;
   static constexpr int kOffSc = kOffA + (A_TMEM ? 0 : ABUF * kABytes);
   static constexpr int kOffBar = kOffSc + SSTAGES * kScBytes;
   static constexpr int kNumBars = 2 * STAGES + 2 * SSTAGES + 2 * ABUF + NP;
@@ -92,6 +94,7 @@ struct Cfg {
   static constexpr int kChunkMax = NMAX - 3;              // rows of a chunk (tile starts 4-aligned)
   static_assert(NMAX % 16 == 0 && NMAX >= 16 && NMAX <= 256, "token tile");
   static_assert(kTokBytes % 1024 == 0 && kOffWpk % 1024 == 0 && kOffA % 1024 == 0, "alignment");
+  static_assert(kOffSc % 128 == 0 && kScBytes % 128 == 0, "TMA destinations 128-byte aligned");
   static_assert(NP * NMAX + (A_TMEM ? ABUF * 32 : 0) <= 512, "tensor memory");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(ABUF % kConvSets == 0 && NP % kConvSets == 0, "each set owns every kConvSets-th buffer");
@@ -102,6 +105,7 @@ struct GemmParams {
   const int64_t* seg;  // [E+1] or nullptr (dense: one expert with M rows)
   uint16_t* C;
   int E, N, K, M;      // M: rows of A (dense) / M_total
+  int gps;             // 128-K groups per stage (divides K/128, <= Cfg::GPS)
 };
 
 // UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -120,25 +124,36 @@ __device__ __forceinline__ uint32_t idesc_e4m3(uint32_t n) {
   return (1u << 4) | ((n >> 3) << 17) | ((128u >> 4) << 24);
 }
 
-// 8 int4 (two's complement nibbles, element i in bits 4i..4i+3) -> 8 E4M3 codes.
-// Positive and negative codes come from two 8-entry tables selected with prmt;
-// a prmt in sign-replicate mode turns each nibble's sign bit into a byte mask.
+// One prepacked 32-bit word (8 weights, see w4a8_prepack_weights) -> 8 E4M3 codes of v + 1/2.
+// Nibble p holds the magnitude index m of element p in bits 0-2 (|v + 1/2| = m + 1/2) and,
+// in bit 3, the sign of element 4 + p/2 (p even) or (p - 1)/2 (p odd): one 8-entry table
+// serves both signs, and the sign bits sit on byte MSBs of w (elements 0-3) or w << 4 (4-7).
 __device__ __forceinline__ void int4x8_to_e4m3x8(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  constexpr uint32_t kPos0 = 0x44403800u;  // E4M3 of 0, 1, 2, 3
-  constexpr uint32_t kPos1 = 0x4E4C4A48u;  //          4, 5, 6, 7
-  constexpr uint32_t kNeg0 = 0xCACCCED0u;  //         -8,-7,-6,-5
-  constexpr uint32_t kNeg1 = 0xB8C0C4C8u;  //         -4,-3,-2,-1
+  constexpr uint32_t kMag0 = 0x46423C30u;  // E4M3 of 0.5, 1.5, 2.5, 3.5
+  constexpr uint32_t kMag1 = 0x4F4D4B49u;  //          4.5, 5.5, 6.5, 7.5
   const uint32_t idx = w & 0x77777777u;
-  const uint32_t idx_hi = idx >> 16;
-  const uint32_t pl = prmt(kPos0, kPos1, idx);
-  const uint32_t nl = prmt(kNeg0, kNeg1, idx);
-  const uint32_t ph = prmt(kPos0, kPos1, idx_hi);
-  const uint32_t nh = prmt(kNeg0, kNeg1, idx_hi);
-  const uint32_t w4 = w << 4;
-  const uint32_t ml = prmt(w4, w, 0xD9C8u);  // byte j = 0xFF if nibble j < 0 (j = 0..3)
-  const uint32_t mh = prmt(w4, w, 0xFBEAu);  // byte j = 0xFF if nibble j+4 < 0
-  lo = (pl & ~ml) | (nl & ml);
-  hi = (ph & ~mh) | (nh & mh);
+  lo = prmt(kMag0, kMag1, idx) | (w & 0x80808080u);
+  hi = prmt(kMag0, kMag1, idx >> 16) | ((w << 4) & 0x80808080u);
+}
+
+// Canonical packed int4 (byte b: element 2b in bits 0-3, 2b+1 in bits 4-7, two's complement)
+// -> the prepacked word above.  Per element: s = sign bit, m = low three bits xor (s ? 7 : 0).
+__global__ void __launch_bounds__(256) prepack_kernel(const uint32_t* __restrict__ in, uint32_t* __restrict__ out,
+                                                      int64_t n_words) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n_words;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint32_t w = in[i];
+    const uint32_t sgn = (w >> 3) & 0x11111111u;         // sign of element i in bit 4i
+    const uint32_t m = (w ^ (sgn * 7u)) & 0x77777777u;     // magnitude index of element i in nibble i
+    // sign of element e goes to bit 3 of nibble 2e+1 (e < 4) or 2(e-4) (e >= 4)
+    uint32_t sb = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int p = e < 4 ? 2 * e + 1 : 2 * (e - 4);
+      sb |= ((sgn >> (4 * e)) & 1u) << (4 * p + 3);
+    }
+    out[i] = m | sb;
+  }
 }
 
 struct Sched {
@@ -194,37 +209,43 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* r) {
   }
 }
 
-// acc[0..1] += (ws * ts[0..1]) * p[0..1], two lanes of fp32 per instruction.
-__device__ __forceinline__ void promote2(float& a0, float& a1, float ws, float t0, float t1, uint32_t p0,
-                                         uint32_t p1) {
-  uint64_t acc, c, ts, w2, pp;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(a0), "f"(a1));
+// acc2 += ws2 * ({t0, t1} * {p0, p1} + {k0, k1}): two fp32 lanes per instruction.  p is
+// the tensor-core partial of (v + 1/2) * a, t the token scale and k = -1/2 * t * sum(a) the
+// group correction, so t * p + k = t * sum(v * a); acc2 and ws2 = {ws, ws} are packed pairs.
+__device__ __forceinline__ void promote2(uint64_t& acc2, uint64_t ws2, float t0, float t1, float k0, float k1,
+                                         uint32_t p0, uint32_t p1) {
+  uint64_t e, ts, ks, pp;
   asm("mov.b64 %0, {%1, %2};" : "=l"(ts) : "f"(t0), "f"(t1));
-  asm("mov.b64 %0, {%1, %1};" : "=l"(w2) : "f"(ws));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ks) : "f"(k0), "f"(k1));
   asm("mov.b64 %0, {%1, %2};" : "=l"(pp) : "r"(p0), "r"(p1));
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(c) : "l"(w2), "l"(ts));
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(c), "l"(pp));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(ts), "l"(pp), "l"(ks));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2) : "l"(ws2), "l"(e));
 }
 
 template <class CF>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(CF::kThreads, 1)
     w4a8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAS,
-                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBS,
-                     const GemmParams prm) {
+                     const __grid_constant__ CUtensorMap tmAC, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmBS, const GemmParams prm) {
   constexpr int NMAX = CF::NMAX;
+  constexpr int GPS = CF::GPS;
   constexpr int STAGES = CF::STAGES;
   constexpr int SSTAGES = CF::SSTAGES;
   constexpr int ABUF = CF::ABUF;
   constexpr int NP = CF::NP;
-  constexpr int NHALF = NMAX / 2;
+  constexpr int kConvSets = CF::kConvSets;
+  constexpr int kEpiWarps = CF::kEpiWarps;
+  constexpr int kWarpConv0 = CF::kWarpConv0;
+  constexpr int kWarpEpi0 = CF::kWarpEpi0;
+  constexpr int NHALF = NMAX * 4 / kEpiWarps;  // columns per epilogue thread
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* s_tok = smem + CF::kOffTok;
-  uint8_t* s_wpk = smem + CF::kOffWpk;
-  uint8_t* s_a = smem + CF::kOffA;
-  uint8_t* s_sc = smem + CF::kOffSc;  // slot: NMAX token scales, then (128-B aligned) 128 weight scales
+  uint8_t* s_tok = smem + CF::kOffTok;  // [STAGES][GPS][NMAX x 128 B]
+  uint8_t* s_wpk = smem + CF::kOffWpk;  // [STAGES][GPS][128 x 64 B]
+  uint8_t* s_a = smem + CF::kOffA;      // [ABUF][128 x 128 B]
+  uint8_t* s_sc = smem + CF::kOffSc;    // [SSTAGES] slot: [GPS][NMAX] token scales, [GPS][NMAX] corrections,
+                                        //   [GPS][128] weight scales
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + CF::kOffBar);
   uint64_t* full = bars;
   uint64_t* empty = full + STAGES;
@@ -241,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = prm.K / kGroup;
+  const int gps = prm.gps;
   const int nblk = prm.N / kBM;
   const int E = prm.seg ? prm.E : 1;
 
@@ -248,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConvWarps + 1);
+      mbar_init(&empty[s], gps * (kConvWarps + 1));  // per group: 4 converter warps + 1 MMA commit
     }
     for (int s = 0; s < SSTAGES; ++s) {
       mbar_init(&sfull[s], 1);
@@ -269,10 +291,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpTma && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmAS);
+    tma_prefetch_desc(&tmAC);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmBS);
   }
-  if (warp == 2) {  // chunk prefix over experts (warp-wide scan)
+  if (warp == kWarpConv0) {  // chunk prefix over experts (warp-wide scan)
     int carry = 0;
     if (lane == 0) s_prefix[0] = 0;
     for (int base = 0; base < E; base += 32) {
@@ -307,30 +330,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   Sched sch{s_prefix, s_start, E, NMAX, nblk};
   const int n_items = s_prefix[E] * nblk;
 
-  // A tile covers rows [row0 & ~3, ...): the scale vectors then start 16-byte aligned.
+  // Counters: `it` counts 128-K groups, `st` counts stages of gps groups; stage st holds
+  // groups [st*gps, st*gps + gps) of one tile (gps divides K/128, so stages never straddle
+  // tiles).  A tile covers token rows [row0 & ~3, ...): the scale vectors start 16-byte aligned.
   if (warp == kWarpTma) {
     if (lane == 0) {
       const uint64_t pol_w = l2_policy_evict_first();
-      uint32_t it = 0;
+      const uint32_t main_bytes = gps * (CF::kTokBytes + CF::kWpkBytes);
+      const uint32_t sc_bytes = gps * (2 * NMAX * 4 + kBM * 4);
+      uint32_t st = 0;
       for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
         int e, nb, row0, rows;
         sch.decode(item, e, nb, row0, rows);
         const int r4 = row0 & ~3;
-        for (int g = 0; g < G; ++g, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
-          const int ss = it % SSTAGES;
-          const uint32_t sph = (it / SSTAGES) & 1;
+        for (int g0 = 0; g0 < G; g0 += gps, ++st) {
+          const int s = st % STAGES;
+          const uint32_t ph = (st / STAGES) & 1;
+          const int ss = st % SSTAGES;
+          const uint32_t sph = (st / SSTAGES) & 1;
           if (!wait_bar(&empty[s], ph ^ 1, s_abort)) goto done;
-          mbar_arrive_expect_tx(&full[s], CF::kTokBytes + CF::kWpkBytes);
-          tma_load_2d(s_tok + s * CF::kTokBytes, &tmA, &full[s], g * kGroup, r4);
-          tma_load_2d_hint(s_wpk + s * CF::kWpkBytes, &tmB, &full[s], g * (kGroup / 2), e * prm.N + nb * kBM,
-                           pol_w);
+          mbar_arrive_expect_tx(&full[s], main_bytes);
+          tma_load_3d(s_tok + s * GPS * CF::kTokBytes, &tmA, &full[s], 0, r4, g0);
+          tma_load_3d_hint(s_wpk + s * GPS * CF::kWpkBytes, &tmB, &full[s], 0, e * prm.N + nb * kBM, g0, pol_w);
           if (!wait_bar(&sempty[ss], sph ^ 1, s_abort)) goto done;
           uint8_t* sc = s_sc + ss * CF::kScBytes;
-          mbar_arrive_expect_tx(&sfull[ss], NMAX * 4 + kBM * 4);
-          tma_load_2d(sc, &tmAS, &sfull[ss], r4, g);
-          tma_load_2d(sc + CF::kWscOff, &tmBS, &sfull[ss], nb * kBM, e * G + g);
+          mbar_arrive_expect_tx(&sfull[ss], sc_bytes);
+          tma_load_2d(sc, &tmAS, &sfull[ss], r4, g0);
+          tma_load_2d(sc + CF::kTscBytes, &tmAC, &sfull[ss], r4, g0);
+          tma_load_2d(sc + 2 * CF::kTscBytes, &tmBS, &sfull[ss], nb * kBM, e * G + g0);
         }
       }
     }
@@ -338,36 +365,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- MMA issue: one thread per group set ----
     const int mset = warp - kWarpMma;
     if (lane == 0) {
-      uint32_t it = 0;
+      uint32_t it = 0, st = 0;
       for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
         int e, nb, row0, rows;
         sch.decode(item, e, nb, row0, rows);
         const int ncol = (row0 - (row0 & ~3) + rows + 15) & ~15;
         const uint32_t idesc = idesc_e4m3(static_cast<uint32_t>(ncol));
-        for (int g = 0; g < G; ++g, ++it) {
-          if (static_cast<int>(it % kConvSets) != mset) continue;
-          const int s = it % STAGES;
-          const int b = it % ABUF;
-          const uint32_t aph = (it / ABUF) & 1;
-          const int pb = it % NP;
-          // mready implies: token tile landed, weights converted, partial buffer free
-          if (!wait_bar(&mready[b], aph, s_abort)) goto done;
-          tc_fence_after();
-          const uint32_t d = tmem_base + pb * NMAX;
-          const uint32_t tok = smem_u32(s_tok + s * CF::kTokBytes);
+        for (int g0 = 0; g0 < G; g0 += gps, ++st) {
+          const int s = st % STAGES;
+          for (int j = 0; j < gps; ++j, ++it) {
+            if (static_cast<int>(it % kConvSets) != mset) continue;
+            const int b = it % ABUF;
+            const uint32_t aph = (it / ABUF) & 1;
+            const int pb = it % NP;
+            // mready implies: token tile landed, weights converted, partial buffer free
+            if (!wait_bar(&mready[b], aph, s_abort)) goto done;
+            tc_fence_after();
+            const uint32_t d = tmem_base + pb * NMAX;
+            const uint32_t tok = smem_u32(s_tok + (s * GPS + j) * CF::kTokBytes);
 #pragma unroll
-          for (int kk = 0; kk < kGroup / kKStep; ++kk) {
-            const uint64_t bdesc = sw128_desc(tok + kk * kKStep);
-            if constexpr (CF::A_TMEM) {
-              const uint32_t a_t = tmem_base + CF::kAColBase + b * 32 + kk * (kKStep / 4);
-              mma_f8f6f4_ts(d, a_t, bdesc, idesc, kk > 0 ? 1u : 0u);
-            } else {
-              const uint64_t adesc = sw128_desc(smem_u32(s_a + b * CF::kABytes) + kk * kKStep);
-              mma_f8f6f4_ss(d, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kGroup / kKStep; ++kk) {
+              const uint64_t bdesc = sw128_desc(tok + kk * kKStep);
+              if constexpr (CF::A_TMEM) {
+                const uint32_t a_t = tmem_base + CF::kAColBase + b * 32 + kk * (kKStep / 4);
+                mma_f8f6f4_ts(d, a_t, bdesc, idesc, kk > 0 ? 1u : 0u);
+              } else {
+                const uint64_t adesc = sw128_desc(smem_u32(s_a + b * CF::kABytes) + kk * kKStep);
+                mma_f8f6f4_ss(d, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+              }
             }
+            mma_commit(&empty[s]);
+            mma_commit(&mdone[b]);
           }
-          mma_commit(&empty[s]);
-          mma_commit(&mdone[b]);
         }
       }
     }
@@ -376,94 +405,105 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q4 = warp & 3;
     const int cset = (warp - kWarpConv0) / kConvWarps;
     const int r = q4 * 32 + lane;
-    uint32_t it = 0;
+    uint32_t it = 0, st = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-      for (int g = 0; g < G; ++g, ++it) {
-        if (static_cast<int>(it % kConvSets) != cset) continue;
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        const int b = it % ABUF;
-        const uint32_t aph = (it / ABUF) & 1;
-        const int pb = it % NP;
-        const uint32_t pph = (it / NP) & 1;
-        const bool ok = wait_bar(&full[s], ph, s_abort) && wait_bar(&mdone[b], aph ^ 1, s_abort) &&
-                        wait_bar(&pempty[pb], pph ^ 1, s_abort);
-        if (__any_sync(0xffffffffu, !ok)) goto done;  // warp-uniform; the warp is converged below
-        const uint8_t* wrow = s_wpk + s * CF::kWpkBytes + r * 64;
-        uint32_t in[16];
+      for (int g0 = 0; g0 < G; g0 += gps, ++st) {
+        const int s = st % STAGES;
+        const uint32_t ph = (st / STAGES) & 1;
+        for (int j = 0; j < gps; ++j, ++it) {
+          if (static_cast<int>(it % kConvSets) != cset) continue;
+          const int b = it % ABUF;
+          const uint32_t aph = (it / ABUF) & 1;
+          const int pb = it % NP;
+          const uint32_t pph = (it / NP) & 1;
+          const bool ok = wait_bar(&full[s], ph, s_abort) && wait_bar(&mdone[b], aph ^ 1, s_abort) &&
+                          wait_bar(&pempty[pb], pph ^ 1, s_abort);
+          if (__any_sync(0xffffffffu, !ok)) goto done;  // warp-uniform; the warp is converged below
+          const uint8_t* wrow = s_wpk + (s * GPS + j) * CF::kWpkBytes + r * 64;
+          uint32_t in[16];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((j ^ ((r >> 1) & 3)) << 4));
-          in[4 * j + 0] = v.x;
-          in[4 * j + 1] = v.y;
-          in[4 * j + 2] = v.z;
-          in[4 * j + 3] = v.w;
+          for (int q = 0; q < 4; ++q) {
+            const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((q ^ ((r >> 1) & 3)) << 4));
+            in[4 * q + 0] = v.x;
+            in[4 * q + 1] = v.y;
+            in[4 * q + 2] = v.z;
+            in[4 * q + 3] = v.w;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
+          uint32_t out[32];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) int4x8_to_e4m3x8(in[i], out[2 * i], out[2 * i + 1]);
+          if constexpr (CF::A_TMEM) {
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + CF::kAColBase + b * 32;
+            tmem_st32(taddr, out);
+            tmem_wait_st();
+            tc_fence_before();
+          } else {
+            uint8_t* arow = s_a + b * CF::kABytes + r * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) =
+                  make_uint4(out[4 * c], out[4 * c + 1], out[4 * c + 2], out[4 * c + 3]);
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&mready[b]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        uint32_t out[32];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) int4x8_to_e4m3x8(in[i], out[2 * i], out[2 * i + 1]);
-        if constexpr (CF::A_TMEM) {
-          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + CF::kAColBase + b * 32;
-          tmem_st32(taddr, out);
-          tmem_wait_st();
-          tc_fence_before();
-        } else {
-          uint8_t* arow = s_a + b * CF::kABytes + r * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) =
-                make_uint4(out[4 * c], out[4 * c + 1], out[4 * c + 2], out[4 * c + 3]);
-          fence_proxy_async_smem();
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&mready[b]);
       }
     }
   } else {
     // ---- promotion and epilogue ----
     const int q4 = warp & 3;
-    const int half = (warp - kWarpEpi0) >> 2;
+    const int half = (warp - kWarpEpi0) >> 2;  // column block of this warp (0 with 4 epilogue warps)
     const int r = q4 * 32 + lane;
     const int c0 = half * NHALF;
     const uint32_t t_lane = static_cast<uint32_t>(q4 * 32) << 16;
     constexpr int CH = NHALF < 16 ? NHALF : 16;
-    uint32_t it = 0;
+    uint32_t it = 0, st = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
       int e, nb, row0, rows;
       sch.decode(item, e, nb, row0, rows);
       const int r4 = row0 & ~3;
       const int lo = row0 - r4;  // columns [lo, lo + rows) of the tile are this chunk's rows
-      float acc[NHALF];
+      uint64_t acc2[NHALF / 2];  // packed pairs of fp32 accumulators
 #pragma unroll
-      for (int j = 0; j < NHALF; ++j) acc[j] = 0.f;
-      for (int g = 0; g < G; ++g, ++it) {
-        const int ss = it % SSTAGES;
-        const uint32_t sph = (it / SSTAGES) & 1;
-        const int pb = it % NP;
-        const int b = it % ABUF;
-        const uint32_t aph = (it / ABUF) & 1;
-        const bool ok = wait_bar(&mdone[b], aph, s_abort) && wait_bar(&sfull[ss], sph, s_abort);
-        if (__any_sync(0xffffffffu, !ok)) goto done;  // warp-uniform; tcgen05.ld needs a converged warp
-        tc_fence_after();
-        const float* sc = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes);
-        const float ws = sc[CF::kWscOff / 4 + r];
+      for (int q = 0; q < NHALF / 2; ++q) acc2[q] = 0ull;
+      for (int g0 = 0; g0 < G; g0 += gps, ++st) {
+        const int ss = st % SSTAGES;
+        const uint32_t sph = (st / SSTAGES) & 1;
+        const float* tsc = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes);
+        const float* tcr = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes + CF::kTscBytes);
+        const float* wsc = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes + 2 * CF::kTscBytes);
+        if (__any_sync(0xffffffffu, !wait_bar(&sfull[ss], sph, s_abort))) goto done;
+        for (int j = 0; j < gps; ++j, ++it) {
+          const int pb = it % NP;
+          const int b = it % ABUF;
+          const uint32_t aph = (it / ABUF) & 1;
+          if (__any_sync(0xffffffffu, !wait_bar(&mdone[b], aph, s_abort))) goto done;  // warp converged below
+          tc_fence_after();
+          const float ws = wsc[j * kBM + r];
+          uint64_t ws2;
+          asm("mov.b64 %0, {%1, %1};" : "=l"(ws2) : "f"(ws));
+          const float* ts = tsc + j * NMAX;
+          const float* tc = tcr + j * NMAX;
 #pragma unroll
-        for (int c = 0; c < NHALF; c += CH) {
-          uint32_t p[CH];
-          tmem_load_cols<CH>(tmem_base + t_lane + pb * NMAX + c0 + c, p);
-          tmem_wait_ld();
-          if (c + CH >= NHALF) {  // last chunk read: hand the buffer back to the MMA
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&pempty[pb]);
-          }
+          for (int c = 0; c < NHALF; c += CH) {
+            uint32_t p[CH];
+            tmem_load_cols<CH>(tmem_base + t_lane + pb * NMAX + c0 + c, p);
+            tmem_wait_ld();
+            if (c + CH >= NHALF) {  // last chunk read: hand the buffer back
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&pempty[pb]);
+            }
 #pragma unroll
-          for (int j = 0; j < CH; j += 4) {
-            const float4 t = *reinterpret_cast<const float4*>(sc + c0 + c + j);
-            promote2(acc[c + j], acc[c + j + 1], ws, t.x, t.y, p[j], p[j + 1]);
-            promote2(acc[c + j + 2], acc[c + j + 3], ws, t.z, t.w, p[j + 2], p[j + 3]);
+            for (int q = 0; q < CH; q += 4) {
+              const float4 t = *reinterpret_cast<const float4*>(ts + c0 + c + q);
+              const float4 k = *reinterpret_cast<const float4*>(tc + c0 + c + q);
+              promote2(acc2[(c + q) / 2], ws2, t.x, t.y, k.x, k.y, p[q], p[q + 1]);
+              promote2(acc2[(c + q) / 2 + 1], ws2, t.z, t.w, k.z, k.w, p[q + 2], p[q + 3]);
+            }
           }
         }
         __syncwarp();
@@ -471,9 +511,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       uint16_t* crow = prm.C + static_cast<int64_t>(r4) * prm.N + nb * kBM + r;
 #pragma unroll
-      for (int j = 0; j < NHALF; ++j) {
-        const int t = c0 + j;
-        if (t >= lo && t < lo + rows) crow[static_cast<int64_t>(t) * prm.N] = float_to_bf16_bits(acc[j]);
+      for (int q = 0; q < NHALF / 2; ++q) {
+        float a0, a1;
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc2[q]));
+        const int t = c0 + 2 * q;
+        if (t >= lo && t < lo + rows) crow[static_cast<int64_t>(t) * prm.N] = float_to_bf16_bits(a0);
+        if (t + 1 >= lo && t + 1 < lo + rows) crow[static_cast<int64_t>(t + 1) * prm.N] = float_to_bf16_bits(a1);
       }
     }
   }
@@ -524,6 +567,21 @@ int make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64
   return W4A8_OK;
 }
 
+int make_map_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, const uint64_t dims[3],
+                const uint64_t strides[2], const uint32_t box[3], CUtensorMapSwizzle sw, const char* name) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return set_error(W4A8_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  const cuuint64_t st[2] = {strides[0], strides[1]};
+  const cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(m, dt, 3, const_cast<void*>(base), d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(W4A8_ERR_INVALID_ARG, "tensor map for %s rejected (CUresult %d)", name, (int)r);
+  return W4A8_OK;
+}
+
 int read_gemm_error() {
   unsigned int v = 0;
   cudaMemcpyFromSymbol(&v, g_gemm_error, sizeof(v));
@@ -537,21 +595,36 @@ struct Registrar {
 } registrar;
 
 template <class CF>
-int launch(const uint8_t* A, const float* a_s, int64_t a_ld, const uint8_t* B, const float* b_s,
+int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, const uint8_t* B, const float* b_s,
            const int64_t* seg, int64_t E, int64_t N, int64_t K, int64_t M, uint16_t* C, cudaStream_t st) {
   const int64_t G = K / kGroup;
-  CUtensorMap tA, tAS, tB, tBS;
+  int gps = 1;  // groups per stage: the largest power of two <= Cfg::GPS dividing K/128
+  while (gps * 2 <= CF::GPS && G % (gps * 2) == 0) gps *= 2;
+  CUtensorMap tA, tAS, tAC, tB, tBS;
   int rc;
-  if ((rc = make_map_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, CF::NMAX,
-                        CU_TENSOR_MAP_SWIZZLE_128B, "A")))
-    return rc;
-  if ((rc = make_map_2d(&tAS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a_s, a_ld, G, a_ld * 4, CF::NMAX, 1,
+  {  // tokens viewed as [group][row][128 B]: one box = gps groups x NMAX rows
+    const uint64_t dims[3] = {128, static_cast<uint64_t>(M), static_cast<uint64_t>(G)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(K), 128};
+    const uint32_t box[3] = {128, static_cast<uint32_t>(CF::NMAX), static_cast<uint32_t>(gps)};
+    if ((rc = make_map_3d(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                          "A")))
+      return rc;
+  }
+  {  // packed weights viewed as [group][row][64 B]: one box = gps groups x 128 rows
+    const uint64_t dims[3] = {64, static_cast<uint64_t>(E * N), static_cast<uint64_t>(G)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(K / 2), 64};
+    const uint32_t box[3] = {64, static_cast<uint32_t>(kBM), static_cast<uint32_t>(gps)};
+    if ((rc = make_map_3d(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B,
+                          "B")))
+      return rc;
+  }
+  if ((rc = make_map_2d(&tAS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a_s, a_ld, G, a_ld * 4, CF::NMAX, gps,
                         CU_TENSOR_MAP_SWIZZLE_NONE, "a_scales")))
     return rc;
-  if ((rc = make_map_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K / 2, E * N, K / 2, 64, kBM,
-                        CU_TENSOR_MAP_SWIZZLE_64B, "B")))
+  if ((rc = make_map_2d(&tAC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a_c, a_ld, G, a_ld * 4, CF::NMAX, gps,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, "a_gcorr")))
     return rc;
-  if ((rc = make_map_2d(&tBS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, b_s, N, E * G, N * 4, kBM, 1,
+  if ((rc = make_map_2d(&tBS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, b_s, N, E * G, N * 4, kBM, gps,
                         CU_TENSOR_MAP_SWIZZLE_NONE, "b_scales")))
     return rc;
   static bool attr_set = false;  // per template instance
@@ -568,16 +641,17 @@ int launch(const uint8_t* A, const float* a_s, int64_t a_ld, const uint8_t* B, c
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
   p.M = static_cast<int>(M);
-  w4a8_gemm_kernel<CF><<<num_sms(), kThreads, CF::kSmemBytes, st>>>(tA, tAS, tB, tBS, p);
+  p.gps = gps;
+  w4a8_gemm_kernel<CF><<<num_sms(), CF::kThreads, CF::kSmemBytes, st>>>(tA, tAS, tAC, tB, tBS, p);
   return check_launch("w4a8_gemm_kernel");
 }
 
 // decode: few rows per expert, weight streaming; converted weights in tensor memory
-using CfgDecode = Cfg<16, 16, 24, 8, 8, true>;
-// prefill: 128-row token tiles, four partial buffers fill tensor memory; weights in shared memory
-using CfgPrefill = Cfg<128, 5, 16, 4, 4, false>;
+using CfgDecode = Cfg<16, 4, 4, 6, 8, 8, true, 2, 4>;
+// prefill: 128-row token tiles; converted weights in tensor memory, two partial buffers
+using CfgPrefill = Cfg<128, 2, 3, 4, 4, 2, true, 1, 8>;
 
-int gemm_common(const uint8_t* A, const float* a_s, int64_t a_ld, const uint8_t* B, const float* b_s,
+int gemm_common(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, const uint8_t* B, const float* b_s,
                 const int64_t* seg, int64_t E, int64_t N, int64_t K, int64_t M, uint16_t* C, void* stream) {
   W4A8_REQUIRE(K > 0 && K % kGroup == 0, "K=%lld must be a positive multiple of 128", (long long)K);
   W4A8_REQUIRE(N > 0 && N % kBM == 0, "N=%lld must be a positive multiple of 128", (long long)N);
@@ -586,35 +660,48 @@ int gemm_common(const uint8_t* A, const float* a_s, int64_t a_ld, const uint8_t*
   W4A8_REQUIRE(E * N < (1ll << 31) && K < (1ll << 31), "E*N or K too large");
   W4A8_REQUIRE(a_ld >= M && a_ld % 4 == 0 && a_ld > 0, "a_scale_ld=%lld must be >= M and a multiple of 4",
                (long long)a_ld);
-  W4A8_REQUIRE(A && a_s && B && b_s && C, "null pointer");
-  W4A8_REQUIRE(aligned16(A) && aligned16(a_s) && aligned16(B) && aligned16(b_s) && aligned16(C),
+  W4A8_REQUIRE(A && a_s && a_c && B && b_s && C, "null pointer");
+  W4A8_REQUIRE(aligned16(A) && aligned16(a_s) && aligned16(a_c) && aligned16(B) && aligned16(b_s) && aligned16(C),
                "device pointers must be 16-byte aligned");
   if (M == 0) return W4A8_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // Few rows per expert: weight streaming, 16-wide token tiles and a deep ring.
   if (M <= 32 * E)
-    return launch<CfgDecode>(A, a_s, a_ld, B, b_s, seg, E, N, K, M, C, st);
-  return launch<CfgPrefill>(A, a_s, a_ld, B, b_s, seg, E, N, K, M, C, st);
+    return launch<CfgDecode>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, st);
+  return launch<CfgPrefill>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, st);
 }
 
 }  // namespace
 }  // namespace w4a8
 
-extern "C" int w4a8_grouped_gemm(const uint8_t* A, const float* a_scales, int64_t a_scale_ld,
-                                 const uint8_t* B_packed, const float* b_scales, const int64_t* seg_indptr,
+extern "C" int w4a8_grouped_gemm(const uint8_t* A, const float* a_scales, const float* a_gcorr, int64_t a_scale_ld,
+                                 const uint8_t* B_prepacked, const float* b_scales, const int64_t* seg_indptr,
                                  int64_t E, int64_t N, int64_t K, int64_t M_total, uint16_t* C, void* ws,
                                  size_t ws_bytes, void* stream) {
   (void)ws;
   (void)ws_bytes;
   W4A8_REQUIRE(seg_indptr != nullptr, "seg_indptr is null");
-  return w4a8::gemm_common(A, a_scales, a_scale_ld, B_packed, b_scales, seg_indptr, E, N, K, M_total, C,
+  return w4a8::gemm_common(A, a_scales, a_gcorr, a_scale_ld, B_prepacked, b_scales, seg_indptr, E, N, K, M_total, C,
                            stream);
 }
 
-extern "C" int w4a8_linear(const uint8_t* A, const float* a_scales, int64_t a_scale_ld, const uint8_t* B_packed,
-                           const float* b_scales, int64_t M, int64_t N, int64_t K, uint16_t* C, void* ws,
-                           size_t ws_bytes, void* stream) {
+extern "C" int w4a8_linear(const uint8_t* A, const float* a_scales, const float* a_gcorr, int64_t a_scale_ld,
+                           const uint8_t* B_prepacked, const float* b_scales, int64_t M, int64_t N, int64_t K,
+                           uint16_t* C, void* ws, size_t ws_bytes, void* stream) {
   (void)ws;
   (void)ws_bytes;
-  return w4a8::gemm_common(A, a_scales, a_scale_ld, B_packed, b_scales, nullptr, 1, N, K, M, C, stream);
+  return w4a8::gemm_common(A, a_scales, a_gcorr, a_scale_ld, B_prepacked, b_scales, nullptr, 1, N, K, M, C, stream);
+}
+
+extern "C" int w4a8_prepack_weights(const uint8_t* w, int64_t rows, int64_t K, uint8_t* out, void* stream) {
+  using namespace w4a8;
+  W4A8_REQUIRE(rows >= 0 && K > 0 && K % 8 == 0, "K=%lld must be a positive multiple of 8", (long long)K);
+  if (rows == 0) return W4A8_OK;
+  W4A8_REQUIRE(w && out, "null pointer");
+  W4A8_REQUIRE(((uintptr_t)w & 3) == 0 && ((uintptr_t)out & 3) == 0, "w and out must be 4-byte aligned");
+  const int64_t n_words = rows * (K / 8);
+  const int64_t blocks = ceil_div(n_words, 256) < 4 * 1184 ? ceil_div(n_words, 256) : 4 * 1184;
+  prepack_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint32_t*>(w), reinterpret_cast<uint32_t*>(out), n_words);
+  return check_launch("prepack_kernel");
 }
