@@ -167,6 +167,25 @@ def ncu_traffic(key):
 
 
 # ---------------------------------------------------------------------------
+# multi-rank aggregation (replicas: every rank runs the whole layer on its own batch)
+
+def reduce_max(value: float, device) -> float:
+    """Max over ranks of a per-rank time (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput(units_per_rank: float, world: int, max_ms: float) -> float:
+    """Whole-job throughput: units processed by all ranks / the slowest rank's time."""
+    return world * units_per_rank / (max_ms / 1e3)
+
+
+# ---------------------------------------------------------------------------
 # our implementation
 
 class MoeRunner:
@@ -294,14 +313,11 @@ def run_ours(args, name, cfg):
     ms = t0.elapsed_time(t1)
     stage_ms = {nm: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)]))
                 for j, (nm, _) in enumerate(st)}
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = reduce_max(ms, dev)
     T, H, I, E, k = r.T, r.H, r.I, r.E, r.k
     P = T * k
     ms_step = ms / K
-    value = world * T * K / (ms / 1e3)
+    value = throughput(T * K, world, ms)
     flops = 2.0 * P * (2 * I * H + I * H)
     w13_bytes = n_touched * (2 * I * H // 2 + 2 * I * (H // 128) * 4)
     w2_bytes = n_touched * (H * I // 2 + H * (I // 128) * 4)
@@ -373,12 +389,8 @@ def e2e_moe(r, args, dev, world):
             raise RuntimeError(r.lib.w4a8_last_error().decode())
     b.record(stream)
     torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    return {"value": round(world * r.T * args.steps / (ms / 1e3), 2), "unit": "tokens/s",
+    ms = reduce_max(a.elapsed_time(b), dev)
+    return {"value": round(throughput(r.T * args.steps, world, ms), 2), "unit": "tokens/s",
             "h2d_bytes_per_step": r.T * r.H * 2 + r.T * r.E * 4, "d2h_bytes_per_step": r.T * r.H * 2,
             "api": "w4a8_moe_forward (one C call) + cudaMemcpyAsync from/to pinned host"}
 
