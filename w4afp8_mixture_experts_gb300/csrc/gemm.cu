@@ -45,8 +45,9 @@ namespace {
 
 constexpr int kBM = 128;      // weight rows per tile (MMA M)
 constexpr int kKStep = 32;    // K per tcgen05.mma for 8-bit operands
-constexpr int kWarpTma = 0;
-constexpr int kWarpMma = 1;                  // warps 1 .. kConvSets issue the MMAs of one set each
+constexpr int kWarpTma = 0;                  // producer of the weight ring
+constexpr int kWarpTmaAct = 1;               // producer of the token and scale rings
+constexpr int kWarpMma = 2;                  // warps 2 .. 1 + kConvSets issue the MMAs of one set each
 constexpr int kConvWarps = 4;                // converter warps per set: one per tensor-memory lane quarter
 constexpr int kMaxExperts = 1024;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s: no legitimate wait comes close
@@ -59,9 +60,12 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
   return p;
 }
 
-template <int NMAX_, int GPS_, int STAGES_, int SSTAGES_, int ABUF_, int NP_, bool A_TMEM_, int SETS_, int EPIW_>
+template <int NMAX_, int GPS_, int STAGES_, int TSTAGES_, int SSTAGES_, int ABUF_, int NP_, bool A_TMEM_, int SETS_,
+          int EPIW_, int PF_>
 struct Cfg {
-  // warp roles: 0 TMA producer | 1..SETS MMA issue | SETS x 4 converters | EPIW epilogue
+  static constexpr int PF = PF_;            // weight stages prefetched into L2 ahead of the shared-memory ring
+  // warp roles: 0 weight producer | 1 token/scale producer | 2..1+SETS MMA issue | SETS x 4 converters |
+  // EPIW epilogue
   static constexpr int kConvSets = SETS_;   // group sets: set c takes the groups with it % SETS == c
   static constexpr int kEpiWarps = EPIW_;   // 4 or 8 (one or two per tensor-memory lane quarter)
   static constexpr int kWarpConv0 = kWarpMma + kConvSets;
@@ -70,7 +74,8 @@ struct Cfg {
   static constexpr int kThreads = kWarps * 32;
   static constexpr int NMAX = NMAX_;        // token tile (MMA N upper bound)
   static constexpr int GPS = GPS_;          // most 128-K groups per pipeline stage
-  static constexpr int STAGES = STAGES_;    // main ring: token tiles + packed weights of GPS groups
+  static constexpr int STAGES = STAGES_;    // weight ring: packed weights of GPS groups (freed by the converters)
+  static constexpr int TSTAGES = TSTAGES_;  // token ring: token tiles of GPS groups (freed by the MMAs)
   static constexpr int SSTAGES = SSTAGES_;  // scale ring: token + weight scales of GPS groups (epilogue)
   static constexpr int ABUF = ABUF_;        // converted weight buffers (one group each)
   static constexpr int NP = NP_;            // fp32 partial-product buffers in tensor memory
@@ -81,14 +86,15 @@ struct Cfg {
   static constexpr int kTscBytes = (GPS * NMAX * 4 + 127) / 128 * 128;  // token scales (and corrections) of a slot
   static constexpr int kScBytes = 2 * kTscBytes + GPS * kBM * 4;        // one scale slot
   static constexpr int kOffTok = 0;
-  static constexpr int kOffWpk = kOffTok + STAGES * GPS * kTokBytes;
+  static constexpr int kOffWpk = kOffTok + TSTAGES * GPS * kTokBytes;
   static constexpr int kOffA = kOffWpk + STAGES * GPS * kWpkBytes;
   static constexpr int kOffSc = kOffA + (A_TMEM ? 0 : ABUF * kABytes);
   static constexpr int kOffBar = kOffSc + SSTAGES * kScBytes;
-  static constexpr int kNumBars = 2 * STAGES + 2 * SSTAGES + 2 * ABUF + NP;
+  static constexpr int kNumBars = 2 * STAGES + 2 * TSTAGES + 2 * SSTAGES + 2 * ABUF + NP;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffSched = kOffMisc + 64;
-  static constexpr int kSmemBytes = kOffSched + 2 * (kMaxExperts + 1) * 4 + 1024;
+  static constexpr int kSmemBytesMax = kOffSched + 2 * (kMaxExperts + 1) * 4 + 1024;
+  static int smem_bytes(int E) { return kOffSched + 2 * (E + 1) * 4 + 1024; }
   static constexpr int kAColBase = NP * NMAX;             // first tensor-memory column of A
   static constexpr uint32_t kTmemCols = pow2_at_least(NP * NMAX + (A_TMEM ? ABUF * 32 : 0));
   static constexpr int kChunkMax = NMAX - 3;              // rows of a chunk (tile starts 4-aligned)
@@ -96,7 +102,7 @@ struct Cfg {
   static_assert(kTokBytes % 1024 == 0 && kOffWpk % 1024 == 0 && kOffA % 1024 == 0, "alignment");
   static_assert(kOffSc % 128 == 0 && kScBytes % 128 == 0, "TMA destinations 128-byte aligned");
   static_assert(NP * NMAX + (A_TMEM ? ABUF * 32 : 0) <= 512, "tensor memory");
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kOffSched + 2 * 257 * 4 + 1024 <= 227 * 1024, "shared memory (256 experts)");
   static_assert(ABUF % kConvSets == 0 && NP % kConvSets == 0, "each set owns every kConvSets-th buffer");
   static_assert(NP <= ABUF, "an A-buffer completion barrier must not run a phase ahead of the epilogue");
 };
@@ -230,6 +236,7 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
   constexpr int NMAX = CF::NMAX;
   constexpr int GPS = CF::GPS;
   constexpr int STAGES = CF::STAGES;
+  constexpr int TSTAGES = CF::TSTAGES;
   constexpr int SSTAGES = CF::SSTAGES;
   constexpr int ABUF = CF::ABUF;
   constexpr int NP = CF::NP;
@@ -241,36 +248,42 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* s_tok = smem + CF::kOffTok;  // [STAGES][GPS][NMAX x 128 B]
+  uint8_t* s_tok = smem + CF::kOffTok;  // [TSTAGES][GPS][NMAX x 128 B]
   uint8_t* s_wpk = smem + CF::kOffWpk;  // [STAGES][GPS][128 x 64 B]
   uint8_t* s_a = smem + CF::kOffA;      // [ABUF][128 x 128 B]
   uint8_t* s_sc = smem + CF::kOffSc;    // [SSTAGES] slot: [GPS][NMAX] token scales, [GPS][NMAX] corrections,
                                         //   [GPS][128] weight scales
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + CF::kOffBar);
-  uint64_t* full = bars;
+  uint64_t* full = bars;                // weight ring
   uint64_t* empty = full + STAGES;
-  uint64_t* sfull = empty + STAGES;
+  uint64_t* tfull = empty + STAGES;     // token ring
+  uint64_t* tempty = tfull + TSTAGES;
+  uint64_t* sfull = tempty + TSTAGES;   // scale ring
   uint64_t* sempty = sfull + SSTAGES;
   uint64_t* mready = sempty + SSTAGES;  // [ABUF] converted weights (and their P buffer) ready for the MMA
   uint64_t* mdone = mready + ABUF;      // [ABUF] MMAs of the group done: A buffer free, partials ready
   uint64_t* pempty = mdone + ABUF;      // [NP] partial buffer read by the epilogue
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + CF::kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + CF::kOffMisc + 4);
-  int* s_prefix = reinterpret_cast<int*>(smem + CF::kOffSched);
-  int* s_start = s_prefix + (kMaxExperts + 1);
+  const int E = prm.seg ? prm.E : 1;
+  int* s_prefix = reinterpret_cast<int*>(smem + CF::kOffSched);  // [E+1]
+  int* s_start = s_prefix + (E + 1);                              // [E+1]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = prm.K / kGroup;
   const int gps = prm.gps;
   const int nblk = prm.N / kBM;
-  const int E = prm.seg ? prm.E : 1;
 
   // ---- prologue: barriers, tensor memory, schedule ----
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], gps * (kConvWarps + 1));  // per group: 4 converter warps + 1 MMA commit
+      mbar_init(&empty[s], gps * kConvWarps);  // per group: the 4 converter warps of its set
+    }
+    for (int s = 0; s < TSTAGES; ++s) {
+      mbar_init(&tfull[s], 1);
+      mbar_init(&tempty[s], gps);  // per group: one MMA commit
     }
     for (int s = 0; s < SSTAGES; ++s) {
       mbar_init(&sfull[s], 1);
@@ -334,9 +347,50 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
   // groups [st*gps, st*gps + gps) of one tile (gps divides K/128, so stages never straddle
   // tiles).  A tile covers token rows [row0 & ~3, ...): the scale vectors start 16-byte aligned.
   if (warp == kWarpTma) {
+    // ---- weight ring producer: runs ahead of everything else ----
     if (lane == 0) {
       const uint64_t pol_w = l2_policy_evict_first();
-      const uint32_t main_bytes = gps * (CF::kTokBytes + CF::kWpkBytes);
+      const uint32_t w_bytes = gps * CF::kWpkBytes;
+      // optional L2 prefetch cursor, CF::PF stages ahead of the shared-memory ring
+      int pf_item = blockIdx.x, pf_g0 = 0, pf_row = 0;
+      auto pf_decode = [&]() {
+        if (pf_item < n_items) {
+          int pe, pnb, pr0, prw;
+          sch.decode(pf_item, pe, pnb, pr0, prw);
+          pf_row = pe * prm.N + pnb * kBM;
+        }
+      };
+      auto pf_step = [&]() {
+        if (pf_item < n_items) tma_prefetch_3d(&tmB, 0, pf_row, pf_g0);
+        pf_g0 += gps;
+        if (pf_g0 >= G) {
+          pf_g0 = 0;
+          pf_item += gridDim.x;
+          pf_decode();
+        }
+      };
+      if (CF::PF > 0) {
+        pf_decode();
+        for (int i = 0; i < CF::PF; ++i) pf_step();
+      }
+      uint32_t st = 0;
+      for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        int e, nb, row0, rows;
+        sch.decode(item, e, nb, row0, rows);
+        for (int g0 = 0; g0 < G; g0 += gps, ++st) {
+          if (CF::PF > 0) pf_step();
+          const int s = st % STAGES;
+          const uint32_t ph = (st / STAGES) & 1;
+          if (!wait_bar(&empty[s], ph ^ 1, s_abort)) goto done;
+          mbar_arrive_expect_tx(&full[s], w_bytes);
+          tma_load_3d_hint(s_wpk + s * GPS * CF::kWpkBytes, &tmB, &full[s], 0, e * prm.N + nb * kBM, g0, pol_w);
+        }
+      }
+    }
+  } else if (warp == kWarpTmaAct) {
+    // ---- token and scale ring producer ----
+    if (lane == 0) {
+      const uint32_t t_bytes = gps * CF::kTokBytes;
       const uint32_t sc_bytes = gps * (2 * NMAX * 4 + kBM * 4);
       uint32_t st = 0;
       for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
@@ -344,14 +398,13 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
         sch.decode(item, e, nb, row0, rows);
         const int r4 = row0 & ~3;
         for (int g0 = 0; g0 < G; g0 += gps, ++st) {
-          const int s = st % STAGES;
-          const uint32_t ph = (st / STAGES) & 1;
+          const int ts_ = st % TSTAGES;
+          const uint32_t tph = (st / TSTAGES) & 1;
           const int ss = st % SSTAGES;
           const uint32_t sph = (st / SSTAGES) & 1;
-          if (!wait_bar(&empty[s], ph ^ 1, s_abort)) goto done;
-          mbar_arrive_expect_tx(&full[s], main_bytes);
-          tma_load_3d(s_tok + s * GPS * CF::kTokBytes, &tmA, &full[s], 0, r4, g0);
-          tma_load_3d_hint(s_wpk + s * GPS * CF::kWpkBytes, &tmB, &full[s], 0, e * prm.N + nb * kBM, g0, pol_w);
+          if (!wait_bar(&tempty[ts_], tph ^ 1, s_abort)) goto done;
+          mbar_arrive_expect_tx(&tfull[ts_], t_bytes);
+          tma_load_3d(s_tok + ts_ * GPS * CF::kTokBytes, &tmA, &tfull[ts_], 0, r4, g0);
           if (!wait_bar(&sempty[ss], sph ^ 1, s_abort)) goto done;
           uint8_t* sc = s_sc + ss * CF::kScBytes;
           mbar_arrive_expect_tx(&sfull[ss], sc_bytes);
@@ -372,13 +425,19 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
         const int ncol = (row0 - (row0 & ~3) + rows + 15) & ~15;
         const uint32_t idesc = idesc_e4m3(static_cast<uint32_t>(ncol));
         for (int g0 = 0; g0 < G; g0 += gps, ++st) {
-          const int s = st % STAGES;
+          const int s = st % TSTAGES;
+          const uint32_t tph = (st / TSTAGES) & 1;
+          bool tok_ready = false;
           for (int j = 0; j < gps; ++j, ++it) {
             if (static_cast<int>(it % kConvSets) != mset) continue;
             const int b = it % ABUF;
             const uint32_t aph = (it / ABUF) & 1;
             const int pb = it % NP;
-            // mready implies: token tile landed, weights converted, partial buffer free
+            if (!tok_ready) {  // once per stage: the token tiles landed
+              if (!wait_bar(&tfull[s], tph, s_abort)) goto done;
+              tok_ready = true;
+            }
+            // mready: weights converted and the partial buffer free
             if (!wait_bar(&mready[b], aph, s_abort)) goto done;
             tc_fence_after();
             const uint32_t d = tmem_base + pb * NMAX;
@@ -394,7 +453,7 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
                 mma_f8f6f4_ss(d, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
               }
             }
-            mma_commit(&empty[s]);
+            mma_commit(&tempty[s]);
             mma_commit(&mdone[b]);
           }
         }
@@ -630,7 +689,7 @@ int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, c
   static bool attr_set = false;  // per template instance
   if (!attr_set) {
     if (cudaFuncSetAttribute(w4a8_gemm_kernel<CF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             CF::kSmemBytes) != cudaSuccess)
+                             CF::kSmemBytesMax) != cudaSuccess)
       return check_launch("cudaFuncSetAttribute(gemm)");
     attr_set = true;
   }
@@ -642,14 +701,15 @@ int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, c
   p.K = static_cast<int>(K);
   p.M = static_cast<int>(M);
   p.gps = gps;
-  w4a8_gemm_kernel<CF><<<num_sms(), CF::kThreads, CF::kSmemBytes, st>>>(tA, tAS, tAC, tB, tBS, p);
+  w4a8_gemm_kernel<CF><<<num_sms(), CF::kThreads, CF::smem_bytes(static_cast<int>(seg ? E : 1)), st>>>(
+      tA, tAS, tAC, tB, tBS, p);
   return check_launch("w4a8_gemm_kernel");
 }
 
 // decode: few rows per expert, weight streaming; converted weights in tensor memory
-using CfgDecode = Cfg<16, 4, 4, 6, 8, 8, true, 2, 4>;
+using CfgDecode = Cfg<16, 4, 5, 4, 6, 8, 8, true, 2, 4, 0>;
 // prefill: 128-row token tiles; converted weights in tensor memory, two partial buffers
-using CfgPrefill = Cfg<128, 2, 3, 4, 4, 2, true, 1, 8>;
+using CfgPrefill = Cfg<128, 2, 4, 3, 4, 4, 2, true, 1, 8, 0>;
 
 int gemm_common(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, const uint8_t* B, const float* b_s,
                 const int64_t* seg, int64_t E, int64_t N, int64_t K, int64_t M, uint16_t* C, void* stream) {
