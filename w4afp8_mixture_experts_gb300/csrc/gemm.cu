@@ -6,30 +6,38 @@
 // group size / chunk_size 128) and, with one expert, the dense W4AFP8 Linear
 // of the lyraW4AFp8 page.
 //
-// Design (one persistent CTA per SM, 14 warps):
+// Design (one persistent CTA per SM; warp roles fixed per configuration):
 //   * Operands are swapped so that the weights fill the 128-row M side of
 //     tcgen05.mma and the few tokens of an expert sit on N (16..NMAX, any
 //     multiple of 16).  Prior art: the swapAB small-batch path of the DeepGEMM
 //     PR #53 page ("SM90 FP4 MegaMoE"); here it is the only mode, and N
 //     shrinks to the expert's rows, so no row tile runs empty.
-//   * warp 0   : TMA producer.  Per 128-K group it loads the token tile (E4M3,
-//                128-byte swizzle), the packed int4 weight tile (64-byte
-//                swizzle), and the fp32 scales of both, into a STAGES-deep ring.
-//   * warps 2-5: converters.  Thread r owns weight row r of the tile, reads its
-//                64 packed bytes and writes 128 E4M3 bytes (int4 -8..7 are all
-//                exact in E4M3) with two 8-entry byte-permute lookups per 8
-//                values, into the UMMA K-major 128-byte-swizzled layout (or into
-//                tensor memory, A_TMEM).
-//   * warp 1   : allocates tensor memory and issues 4 MMAs (K = 32 each) per
-//                group into one of two fp32 accumulators P in tensor memory.
-//   * warps 6-13: promotion.  The scales differ per 128-K group, so each
-//                group's partial product leaves the tensor core (tcgen05.ld)
-//                and is added in fp32: acc += (w_s * a_s) * P (the epilogue
-//                FFMA promotion the DeepGEMM PR #53 page describes for SM90,
-//                kept here because the scales are arbitrary fp32 values).  The
-//                second P buffer lets the tensor core run the next group
-//                meanwhile.  At the end of a tile the accumulators are rounded
-//                to bf16 and stored.
+//   * The K loop runs in stages of gps 128-K groups of one tile.  A stage is
+//     the unit of every barrier transaction below, so the fixed cost of a
+//     hand-over (waits, fences, arrivals) is paid once per gps groups.
+//   * warp 0: weight producer.  TMA loads the prepacked int4 tile of a stage
+//     (64-byte swizzle, L2 evict-first) into a STAGES-deep ring.
+//   * warp 1: token and scale producer.  TMA loads the E4M3 token tiles
+//     (128-byte swizzle) into a TSTAGES ring and the fp32 token scales, group
+//     corrections and weight scales into an SSTAGES ring.
+//   * SETS x 4 converter warps: thread r owns weight row r, reads its 64
+//     packed bytes per group and writes 128 E4M3 bytes of v + 1/2 (7 integer
+//     operations per 8 weights, two 8-entry byte-permute lookups) into tensor
+//     memory (A_TMEM) or the UMMA K-major 128-byte-swizzled shared layout.
+//   * MMAS MMA warps: one thread each issues 4 tcgen05.mma (K = 32) per group
+//     into that group's fp32 partial P in tensor memory.  An issuing thread
+//     stalls about 120 cycles per tcgen05.mma whatever N is, so several warps
+//     issue, each owning every MMAS-th stage.
+//   * epilogue warps: the scales differ per 128-K group, so each group's P
+//     leaves the tensor core (tcgen05.ld) and is promoted in fp32:
+//     acc += w_s * (a_s * P + gcorr), gcorr = -1/2 * a_s * sum(a) undoing the
+//     +1/2 of the weight codes (the epilogue FFMA promotion the DeepGEMM PR #53
+//     page describes for SM90, kept because the scales are arbitrary fp32
+//     values).  At the end of a tile the accumulators are rounded to bf16.
+//   * Every barrier slot is waited on by exactly one warp (set) per role, which
+//     meets the slot's phases in order: the ring depths are multiples of the
+//     set counts (static_asserts in Cfg), the condition under which a
+//     phase-parity wait cannot be satisfied by a stale phase.
 //   * Tiles: (expert, token chunk, 128-row weight block); chunks split an
 //     expert's rows evenly into pieces of at most NMAX; the schedule is built
 //     in shared memory from seg_indptr by every CTA (no host synchronisation,
@@ -47,7 +55,7 @@ constexpr int kBM = 128;      // weight rows per tile (MMA M)
 constexpr int kKStep = 32;    // K per tcgen05.mma for 8-bit operands
 constexpr int kWarpTma = 0;                  // producer of the weight ring
 constexpr int kWarpTmaAct = 1;               // producer of the token and scale rings
-constexpr int kWarpMma = 2;                  // warps 2 .. 1 + kConvSets issue the MMAs of one set each
+constexpr int kWarpMma = 2;                  // warps 2 .. 1 + kMmaWarps issue the MMAs
 constexpr int kConvWarps = 4;                // converter warps per set: one per tensor-memory lane quarter
 constexpr int kMaxExperts = 1024;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s: no legitimate wait comes close
@@ -60,25 +68,31 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
   return p;
 }
 
+// Every consumer works on whole pipeline stages (GPS 128-K groups of one tile): a stage is
+// one barrier transaction for the converters, the MMA issue and the epilogue.
 template <int NMAX_, int GPS_, int STAGES_, int TSTAGES_, int SSTAGES_, int ABUF_, int NP_, bool A_TMEM_, int SETS_,
-          int EPIW_, int PF_>
+          int MMAS_, int EPIW_, int EPIS_>
 struct Cfg {
-  static constexpr int PF = PF_;            // weight stages prefetched into L2 ahead of the shared-memory ring
-  // warp roles: 0 weight producer | 1 token/scale producer | 2..1+SETS MMA issue | SETS x 4 converters |
+  // warp roles: 0 weight producer | 1 token/scale producer | 2..1+MMAS MMA issue | SETS x 4 converters |
   // EPIW epilogue
-  static constexpr int kConvSets = SETS_;   // group sets: set c takes the groups with it % SETS == c
-  static constexpr int kEpiWarps = EPIW_;   // 4 or 8 (one or two per tensor-memory lane quarter)
-  static constexpr int kWarpConv0 = kWarpMma + kConvSets;
+  static constexpr int kConvSets = SETS_;   // converter sets: set c converts the stages with st % SETS == c
+  static constexpr int kMmaWarps = MMAS_;   // MMA warps: warp m issues the stages with st % MMAS == m (a
+                                            // thread stalls ~120 cycles per tcgen05.mma, so several
+                                            // issuing warps keep the tensor core fed)
+  static constexpr int kEpiWarps = EPIW_;   // 4 x column blocks x epilogue sets
+  static constexpr int kEpiSets = EPIS_;    // epilogue sets: set c promotes the stages with st % EPIS == c
+  static constexpr int kEpiSetWarps = EPIW_ / EPIS_;  // warps of one epilogue set (4 x column blocks)
+  static constexpr int kWarpConv0 = kWarpMma + kMmaWarps;
   static constexpr int kWarpEpi0 = kWarpConv0 + kConvSets * kConvWarps;
   static constexpr int kWarps = kWarpEpi0 + kEpiWarps;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int NMAX = NMAX_;        // token tile (MMA N upper bound)
   static constexpr int GPS = GPS_;          // most 128-K groups per pipeline stage
-  static constexpr int STAGES = STAGES_;    // weight ring: packed weights of GPS groups (freed by the converters)
-  static constexpr int TSTAGES = TSTAGES_;  // token ring: token tiles of GPS groups (freed by the MMAs)
-  static constexpr int SSTAGES = SSTAGES_;  // scale ring: token + weight scales of GPS groups (epilogue)
-  static constexpr int ABUF = ABUF_;        // converted weight buffers (one group each)
-  static constexpr int NP = NP_;            // fp32 partial-product buffers in tensor memory
+  static constexpr int STAGES = STAGES_;    // weight ring: packed weights of a stage (freed by the converters)
+  static constexpr int TSTAGES = TSTAGES_;  // token ring: token tiles of a stage (freed by the MMAs)
+  static constexpr int SSTAGES = SSTAGES_;  // scale ring: token + weight scales of a stage (epilogue)
+  static constexpr int ABUF = ABUF_;        // converted-weight slots (one stage each)
+  static constexpr int NP = NP_;            // fp32 partial-product slots in tensor memory (one stage each)
   static constexpr bool A_TMEM = A_TMEM_;   // converted weights in tensor memory (else shared)
   static constexpr int kTokBytes = NMAX * 128;            // one group: NMAX rows x 128 B, 128B swizzle
   static constexpr int kWpkBytes = kBM * 64;              // one group: 128 rows x 64 B packed int4
@@ -88,23 +102,34 @@ struct Cfg {
   static constexpr int kOffTok = 0;
   static constexpr int kOffWpk = kOffTok + TSTAGES * GPS * kTokBytes;
   static constexpr int kOffA = kOffWpk + STAGES * GPS * kWpkBytes;
-  static constexpr int kOffSc = kOffA + (A_TMEM ? 0 : ABUF * kABytes);
+  static constexpr int kOffSc = kOffA + (A_TMEM ? 0 : ABUF * GPS * kABytes);
   static constexpr int kOffBar = kOffSc + SSTAGES * kScBytes;
-  static constexpr int kNumBars = 2 * STAGES + 2 * TSTAGES + 2 * SSTAGES + 2 * ABUF + NP;
+  static constexpr int kNumBars = 2 * STAGES + 2 * TSTAGES + 2 * SSTAGES + 2 * ABUF + NP + 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffSched = kOffMisc + 64;
   static constexpr int kSmemBytesMax = kOffSched + 2 * (kMaxExperts + 1) * 4 + 1024;
   static int smem_bytes(int E) { return kOffSched + 2 * (E + 1) * 4 + 1024; }
-  static constexpr int kAColBase = NP * NMAX;             // first tensor-memory column of A
-  static constexpr uint32_t kTmemCols = pow2_at_least(NP * NMAX + (A_TMEM ? ABUF * 32 : 0));
+  // tensor memory: [NP][GPS][NMAX] partials | [ABUF][GPS][32] converted weights (A_TMEM) |
+  // with two epilogue sets, two NMAX-column slots (by tile parity) through which set 1 hands
+  // its accumulators to set 0 at the end of a tile
+  static constexpr int kAColBase = NP * GPS * NMAX;
+  static constexpr int kXColBase = (kAColBase + (A_TMEM ? ABUF * GPS * 32 : 0) + 31) / 32 * 32;
+  static constexpr int kTmemUsed = kXColBase + (EPIS_ > 1 ? 2 * NMAX : 0);
+  static constexpr uint32_t kTmemCols = pow2_at_least(kTmemUsed);
   static constexpr int kChunkMax = NMAX - 3;              // rows of a chunk (tile starts 4-aligned)
   static_assert(NMAX % 16 == 0 && NMAX >= 16 && NMAX <= 256, "token tile");
   static_assert(kTokBytes % 1024 == 0 && kOffWpk % 1024 == 0 && kOffA % 1024 == 0, "alignment");
   static_assert(kOffSc % 128 == 0 && kScBytes % 128 == 0, "TMA destinations 128-byte aligned");
-  static_assert(NP * NMAX + (A_TMEM ? ABUF * 32 : 0) <= 512, "tensor memory");
+  static_assert(kTmemUsed <= 512, "tensor memory");
+  static_assert(EPIS_ == 1 || EPIS_ == 2, "one or two epilogue sets");
+  static_assert(EPIW_ % (4 * EPIS_) == 0, "each epilogue set covers all four lane quarters");
   static_assert(kOffSched + 2 * 257 * 4 + 1024 <= 227 * 1024, "shared memory (256 experts)");
-  static_assert(ABUF % kConvSets == 0 && NP % kConvSets == 0, "each set owns every kConvSets-th buffer");
-  static_assert(NP <= ABUF, "an A-buffer completion barrier must not run a phase ahead of the epilogue");
+  static_assert(NP <= ABUF, "an A-slot completion barrier must not run a phase ahead of the epilogue");
+  // Every barrier slot must be waited on by one warp (set) of each role, which then meets the
+  // slot's phases in order; a phase-parity wait is only unambiguous under that condition.
+  static_assert(STAGES % SETS_ == 0 && ABUF % SETS_ == 0 && NP % SETS_ == 0, "converter sets own whole slots");
+  static_assert(ABUF % MMAS_ == 0 && TSTAGES % MMAS_ == 0, "MMA warps own whole slots");
+  static_assert(SSTAGES % EPIS_ == 0 && ABUF % EPIS_ == 0 && NP % EPIS_ == 0, "epilogue sets own whole slots");
 };
 
 struct GemmParams {
@@ -241,10 +266,10 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
   constexpr int ABUF = CF::ABUF;
   constexpr int NP = CF::NP;
   constexpr int kConvSets = CF::kConvSets;
-  constexpr int kEpiWarps = CF::kEpiWarps;
+  constexpr int EPIS = CF::kEpiSets;
   constexpr int kWarpConv0 = CF::kWarpConv0;
   constexpr int kWarpEpi0 = CF::kWarpEpi0;
-  constexpr int NHALF = NMAX * 4 / kEpiWarps;  // columns per epilogue thread
+  constexpr int NHALF = NMAX * 4 / CF::kEpiSetWarps;  // columns per epilogue thread
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -263,6 +288,8 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
   uint64_t* mready = sempty + SSTAGES;  // [ABUF] converted weights (and their P buffer) ready for the MMA
   uint64_t* mdone = mready + ABUF;      // [ABUF] MMAs of the group done: A buffer free, partials ready
   uint64_t* pempty = mdone + ABUF;      // [NP] partial buffer read by the epilogue
+  uint64_t* xfull = pempty + NP;        // [2] epilogue set 1 -> set 0 hand-over slot written
+  uint64_t* xempty = xfull + 2;         // [2] hand-over slot read
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + CF::kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + CF::kOffMisc + 4);
   const int E = prm.seg ? prm.E : 1;
@@ -279,21 +306,25 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], gps * kConvWarps);  // per group: the 4 converter warps of its set
+      mbar_init(&empty[s], kConvWarps);  // the 4 converter warps of the stage's set
     }
     for (int s = 0; s < TSTAGES; ++s) {
       mbar_init(&tfull[s], 1);
-      mbar_init(&tempty[s], gps);  // per group: one MMA commit
+      mbar_init(&tempty[s], 1);  // the stage's MMA commit
     }
     for (int s = 0; s < SSTAGES; ++s) {
       mbar_init(&sfull[s], 1);
-      mbar_init(&sempty[s], kEpiWarps);
+      mbar_init(&sempty[s], CF::kEpiSetWarps);  // the warps of the stage's epilogue set
     }
     for (int b = 0; b < ABUF; ++b) {
       mbar_init(&mready[b], kConvWarps);
       mbar_init(&mdone[b], 1);
     }
-    for (int b = 0; b < NP; ++b) mbar_init(&pempty[b], kEpiWarps);
+    for (int b = 0; b < NP; ++b) mbar_init(&pempty[b], CF::kEpiSetWarps);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&xfull[b], CF::kEpiSetWarps);
+      mbar_init(&xempty[b], CF::kEpiSetWarps);
+    }
     *s_abort = 0;
     mbar_fence_init();
   }
@@ -351,34 +382,11 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_w = l2_policy_evict_first();
       const uint32_t w_bytes = gps * CF::kWpkBytes;
-      // optional L2 prefetch cursor, CF::PF stages ahead of the shared-memory ring
-      int pf_item = blockIdx.x, pf_g0 = 0, pf_row = 0;
-      auto pf_decode = [&]() {
-        if (pf_item < n_items) {
-          int pe, pnb, pr0, prw;
-          sch.decode(pf_item, pe, pnb, pr0, prw);
-          pf_row = pe * prm.N + pnb * kBM;
-        }
-      };
-      auto pf_step = [&]() {
-        if (pf_item < n_items) tma_prefetch_3d(&tmB, 0, pf_row, pf_g0);
-        pf_g0 += gps;
-        if (pf_g0 >= G) {
-          pf_g0 = 0;
-          pf_item += gridDim.x;
-          pf_decode();
-        }
-      };
-      if (CF::PF > 0) {
-        pf_decode();
-        for (int i = 0; i < CF::PF; ++i) pf_step();
-      }
       uint32_t st = 0;
       for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
         int e, nb, row0, rows;
         sch.decode(item, e, nb, row0, rows);
         for (int g0 = 0; g0 < G; g0 += gps, ++st) {
-          if (CF::PF > 0) pf_step();
           const int s = st % STAGES;
           const uint32_t ph = (st / STAGES) & 1;
           if (!wait_bar(&empty[s], ph ^ 1, s_abort)) goto done;
@@ -415,69 +423,70 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
       }
     }
   } else if (warp < kWarpConv0) {
-    // ---- MMA issue: one thread per group set ----
+    // ---- MMA issue: warp m issues the stages with st % kMmaWarps == m ----
     const int mset = warp - kWarpMma;
     if (lane == 0) {
-      uint32_t it = 0, st = 0;
+      uint32_t st = 0;
       for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
         int e, nb, row0, rows;
         sch.decode(item, e, nb, row0, rows);
         const int ncol = (row0 - (row0 & ~3) + rows + 15) & ~15;
         const uint32_t idesc = idesc_e4m3(static_cast<uint32_t>(ncol));
         for (int g0 = 0; g0 < G; g0 += gps, ++st) {
-          const int s = st % TSTAGES;
+          if (static_cast<int>(st % CF::kMmaWarps) != mset) continue;
+          const int ts_ = st % TSTAGES;
           const uint32_t tph = (st / TSTAGES) & 1;
-          bool tok_ready = false;
-          for (int j = 0; j < gps; ++j, ++it) {
-            if (static_cast<int>(it % kConvSets) != mset) continue;
-            const int b = it % ABUF;
-            const uint32_t aph = (it / ABUF) & 1;
-            const int pb = it % NP;
-            if (!tok_ready) {  // once per stage: the token tiles landed
-              if (!wait_bar(&tfull[s], tph, s_abort)) goto done;
-              tok_ready = true;
-            }
-            // mready: weights converted and the partial buffer free
-            if (!wait_bar(&mready[b], aph, s_abort)) goto done;
-            tc_fence_after();
-            const uint32_t d = tmem_base + pb * NMAX;
-            const uint32_t tok = smem_u32(s_tok + (s * GPS + j) * CF::kTokBytes);
+          const int a = st % ABUF;
+          const uint32_t aph = (st / ABUF) & 1;
+          const int pslot = st % NP;
+          // token tiles landed; weights converted (and their partial slot free)
+          if (!wait_bar(&tfull[ts_], tph, s_abort) || !wait_bar(&mready[a], aph, s_abort)) goto done;
+          tc_fence_after();
+#pragma unroll
+          for (int j = 0; j < GPS; ++j) {
+            if (j >= gps) break;
+            const uint32_t d = tmem_base + (pslot * GPS + j) * NMAX;
+            const uint32_t tok = smem_u32(s_tok + (ts_ * GPS + j) * CF::kTokBytes);
 #pragma unroll
             for (int kk = 0; kk < kGroup / kKStep; ++kk) {
               const uint64_t bdesc = sw128_desc(tok + kk * kKStep);
               if constexpr (CF::A_TMEM) {
-                const uint32_t a_t = tmem_base + CF::kAColBase + b * 32 + kk * (kKStep / 4);
+                const uint32_t a_t = tmem_base + CF::kAColBase + (a * GPS + j) * 32 + kk * (kKStep / 4);
                 mma_f8f6f4_ts(d, a_t, bdesc, idesc, kk > 0 ? 1u : 0u);
               } else {
-                const uint64_t adesc = sw128_desc(smem_u32(s_a + b * CF::kABytes) + kk * kKStep);
+                const uint64_t adesc = sw128_desc(smem_u32(s_a + (a * GPS + j) * CF::kABytes) + kk * kKStep);
                 mma_f8f6f4_ss(d, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
               }
             }
-            mma_commit(&tempty[s]);
-            mma_commit(&mdone[b]);
           }
+          mma_commit(&tempty[ts_]);
+          mma_commit(&mdone[a]);
         }
       }
     }
   } else if (warp < kWarpEpi0) {
-    // ---- converters: int4 -> E4M3; set `cset` takes every kConvSets-th group ----
+    // ---- converters: int4 -> E4M3; set `cset` converts the stages with st % kConvSets == cset ----
     const int q4 = warp & 3;
     const int cset = (warp - kWarpConv0) / kConvWarps;
     const int r = q4 * 32 + lane;
-    uint32_t it = 0, st = 0;
+    uint32_t st = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
       for (int g0 = 0; g0 < G; g0 += gps, ++st) {
+        if (static_cast<int>(st % kConvSets) != cset) continue;
         const int s = st % STAGES;
         const uint32_t ph = (st / STAGES) & 1;
-        for (int j = 0; j < gps; ++j, ++it) {
-          if (static_cast<int>(it % kConvSets) != cset) continue;
-          const int b = it % ABUF;
-          const uint32_t aph = (it / ABUF) & 1;
-          const int pb = it % NP;
-          const uint32_t pph = (it / NP) & 1;
-          const bool ok = wait_bar(&full[s], ph, s_abort) && wait_bar(&mdone[b], aph ^ 1, s_abort) &&
-                          wait_bar(&pempty[pb], pph ^ 1, s_abort);
-          if (__any_sync(0xffffffffu, !ok)) goto done;  // warp-uniform; the warp is converged below
+        const int a = st % ABUF;
+        const uint32_t aph = (st / ABUF) & 1;
+        const int pslot = st % NP;
+        const uint32_t pph = (st / NP) & 1;
+        // weights landed, the A slot's previous MMAs done, the partial slot read by the epilogue
+        const bool ok = mbar_test3(&full[s], ph, &mdone[a], aph ^ 1, &pempty[pslot], pph ^ 1) ||
+                        (wait_bar(&full[s], ph, s_abort) && wait_bar(&mdone[a], aph ^ 1, s_abort) &&
+                         wait_bar(&pempty[pslot], pph ^ 1, s_abort));
+        if (__any_sync(0xffffffffu, !ok)) goto done;  // warp-uniform; the warp is converged below
+#pragma unroll
+        for (int j = 0; j < GPS; ++j) {
+          if (j >= gps) break;
           const uint8_t* wrow = s_wpk + (s * GPS + j) * CF::kWpkBytes + r * 64;
           uint32_t in[16];
 #pragma unroll
@@ -488,59 +497,69 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
             in[4 * q + 2] = v.z;
             in[4 * q + 3] = v.w;
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[s]);
           uint32_t out[32];
 #pragma unroll
           for (int i = 0; i < 16; ++i) int4x8_to_e4m3x8(in[i], out[2 * i], out[2 * i + 1]);
           if constexpr (CF::A_TMEM) {
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + CF::kAColBase + b * 32;
-            tmem_st32(taddr, out);
-            tmem_wait_st();
-            tc_fence_before();
+            tmem_st32(tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + CF::kAColBase + (a * GPS + j) * 32, out);
           } else {
-            uint8_t* arow = s_a + b * CF::kABytes + r * 128;
+            uint8_t* arow = s_a + (a * GPS + j) * CF::kABytes + r * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c)
               *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) =
                   make_uint4(out[4 * c], out[4 * c + 1], out[4 * c + 2], out[4 * c + 3]);
-            fence_proxy_async_smem();
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&mready[b]);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // every packed byte of the stage is in registers by now
+        if constexpr (CF::A_TMEM) {
+          tmem_wait_st();
+          tc_fence_before();
+        } else {
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&mready[a]);
       }
     }
   } else {
     // ---- promotion and epilogue ----
+    // Warp w: lane quarter q4 = w & 3, epilogue set `eset` (the stages with st % EPIS == eset)
+    // and, within the set, column block `half`.
+    const int ew = warp - kWarpEpi0;
     const int q4 = warp & 3;
-    const int half = (warp - kWarpEpi0) >> 2;  // column block of this warp (0 with 4 epilogue warps)
+    const int eset = ew / CF::kEpiSetWarps;
+    const int half = (ew % CF::kEpiSetWarps) >> 2;
     const int r = q4 * 32 + lane;
     const int c0 = half * NHALF;
     const uint32_t t_lane = static_cast<uint32_t>(q4 * 32) << 16;
-    constexpr int CH = NHALF < 16 ? NHALF : 16;
-    uint32_t it = 0, st = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    constexpr int CH = NHALF < 16 ? 8 : 16;  // columns per tensor-memory load
+    uint32_t st = 0, tile = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++tile) {
       int e, nb, row0, rows;
       sch.decode(item, e, nb, row0, rows);
       const int r4 = row0 & ~3;
-      const int lo = row0 - r4;  // columns [lo, lo + rows) of the tile are this chunk's rows
-      uint64_t acc2[NHALF / 2];  // packed pairs of fp32 accumulators
+      const int lo = row0 - r4;   // columns [lo, lo + rows) of the tile are this chunk's rows
+      const int need = lo + rows;  // columns past `need` are never stored: skip their promotion
+      uint64_t acc2[NHALF / 2];   // packed pairs of fp32 accumulators
 #pragma unroll
       for (int q = 0; q < NHALF / 2; ++q) acc2[q] = 0ull;
       for (int g0 = 0; g0 < G; g0 += gps, ++st) {
+        if (EPIS > 1 && static_cast<int>(st % EPIS) != eset) continue;
         const int ss = st % SSTAGES;
         const uint32_t sph = (st / SSTAGES) & 1;
+        const int a = st % ABUF;
+        const uint32_t aph = (st / ABUF) & 1;
+        const int pslot = st % NP;
         const float* tsc = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes);
         const float* tcr = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes + CF::kTscBytes);
         const float* wsc = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes + 2 * CF::kTscBytes);
-        if (__any_sync(0xffffffffu, !wait_bar(&sfull[ss], sph, s_abort))) goto done;
-        for (int j = 0; j < gps; ++j, ++it) {
-          const int pb = it % NP;
-          const int b = it % ABUF;
-          const uint32_t aph = (it / ABUF) & 1;
-          if (__any_sync(0xffffffffu, !wait_bar(&mdone[b], aph, s_abort))) goto done;  // warp converged below
-          tc_fence_after();
+        const bool ok = wait_bar(&sfull[ss], sph, s_abort) && wait_bar(&mdone[a], aph, s_abort);
+        if (__any_sync(0xffffffffu, !ok)) goto done;  // warp converged below
+        tc_fence_after();
+#pragma unroll
+        for (int j = 0; j < GPS; ++j) {
+          if (j >= gps) break;
           const float ws = wsc[j * kBM + r];
           uint64_t ws2;
           asm("mov.b64 %0, {%1, %1};" : "=l"(ws2) : "f"(ws));
@@ -548,14 +567,10 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
           const float* tc = tcr + j * NMAX;
 #pragma unroll
           for (int c = 0; c < NHALF; c += CH) {
+            if (c0 + c >= need) continue;  // warp-uniform
             uint32_t p[CH];
-            tmem_load_cols<CH>(tmem_base + t_lane + pb * NMAX + c0 + c, p);
+            tmem_load_cols<CH>(tmem_base + t_lane + (pslot * GPS + j) * NMAX + c0 + c, p);
             tmem_wait_ld();
-            if (c + CH >= NHALF) {  // last chunk read: hand the buffer back
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&pempty[pb]);
-            }
 #pragma unroll
             for (int q = 0; q < CH; q += 4) {
               const float4 t = *reinterpret_cast<const float4*>(ts + c0 + c + q);
@@ -565,8 +580,53 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
             }
           }
         }
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sempty[ss]);
+        if (lane == 0) {
+          mbar_arrive(&pempty[pslot]);
+          mbar_arrive(&sempty[ss]);
+        }
+      }
+      if constexpr (EPIS > 1) {
+        // Set 1 hands its partial sums to set 0 through tensor memory (same lane quarter and
+        // columns); slot = tile parity, guarded by xfull / xempty.
+        const int xs = tile & 1;
+        const uint32_t xph = (tile >> 1) & 1;
+        const uint32_t xaddr = tmem_base + t_lane + CF::kXColBase + xs * NMAX + c0;
+        if (eset != 0) {
+          if (__any_sync(0xffffffffu, !wait_bar(&xempty[xs], xph ^ 1, s_abort))) goto done;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < NHALF; c += 8) {
+            uint32_t v[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              asm("mov.b64 {%0, %1}, %2;" : "=r"(v[2 * q]), "=r"(v[2 * q + 1]) : "l"(acc2[c / 2 + q]));
+            tmem_st8(xaddr + c, v);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&xfull[xs]);
+          continue;
+        }
+        if (__any_sync(0xffffffffu, !wait_bar(&xfull[xs], xph, s_abort))) goto done;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < NHALF; c += 8) {
+          uint32_t v[8];
+          tmem_ld8(xaddr + c, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint64_t o;
+            asm("mov.b64 %0, {%1, %2};" : "=l"(o) : "r"(v[2 * q]), "r"(v[2 * q + 1]));
+            asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc2[c / 2 + q]) : "l"(o));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xempty[xs]);
       }
       uint16_t* crow = prm.C + static_cast<int64_t>(r4) * prm.N + nb * kBM + r;
 #pragma unroll
@@ -707,9 +767,9 @@ int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, c
 }
 
 // decode: few rows per expert, weight streaming; converted weights in tensor memory
-using CfgDecode = Cfg<16, 4, 5, 4, 6, 8, 8, true, 2, 4, 0>;
-// prefill: 128-row token tiles; converted weights in tensor memory, two partial buffers
-using CfgPrefill = Cfg<128, 2, 4, 3, 4, 4, 2, true, 1, 8, 0>;
+using CfgDecode = Cfg<16, 2, 10, 8, 12, 4, 4, true, 2, 2, 4, 1>;
+// prefill: 128-row token tiles, one group per stage; converted weights in tensor memory
+using CfgPrefill = Cfg<128, 1, 8, 6, 8, 4, 2, true, 1, 2, 8, 1>;
 
 int gemm_common(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, const uint8_t* B, const float* b_s,
                 const int64_t* seg, int64_t E, int64_t N, int64_t K, int64_t M, uint16_t* C, void* stream) {
