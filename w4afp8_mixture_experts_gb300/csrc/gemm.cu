@@ -26,18 +26,18 @@
 //     memory (A_TMEM) or the UMMA K-major 128-byte-swizzled shared layout.
 //   * MMAS MMA warps: one thread each issues 4 tcgen05.mma (K = 32) per group
 //     into that group's fp32 partial P in tensor memory.  An issuing thread
-//     stalls about 120 cycles per tcgen05.mma whatever N is, so several warps
-//     issue, each owning every MMAS-th stage.
+//     stalls about 120 cycles per tcgen05.mma whatever N is, so the groups of
+//     a stage are dealt out to several issuing warps.
 //   * epilogue warps: the scales differ per 128-K group, so each group's P
 //     leaves the tensor core (tcgen05.ld) and is promoted in fp32:
 //     acc += w_s * (a_s * P + gcorr), gcorr = -1/2 * a_s * sum(a) undoing the
 //     +1/2 of the weight codes (the epilogue FFMA promotion the DeepGEMM PR #53
 //     page describes for SM90, kept because the scales are arbitrary fp32
 //     values).  At the end of a tile the accumulators are rounded to bf16.
-//   * Every barrier slot is waited on by exactly one warp (set) per role, which
-//     meets the slot's phases in order: the ring depths are multiples of the
-//     set counts (static_asserts in Cfg), the condition under which a
-//     phase-parity wait cannot be satisfied by a stale phase.
+//   * Every role walks all stages in order, splitting a stage's groups among
+//     its warps, so each barrier's waiters meet its phases in order: the
+//     condition under which a phase-parity wait cannot be satisfied by a stale
+//     phase.
 //   * Tiles: (expert, token chunk, 128-row weight block); chunks split an
 //     expert's rows evenly into pieces of at most NMAX; the schedule is built
 //     in shared memory from seg_indptr by every CTA (no host synchronisation,
@@ -75,12 +75,12 @@ template <int NMAX_, int GPS_, int STAGES_, int TSTAGES_, int SSTAGES_, int ABUF
 struct Cfg {
   // warp roles: 0 weight producer | 1 token/scale producer | 2..1+MMAS MMA issue | SETS x 4 converters |
   // EPIW epilogue
-  static constexpr int kConvSets = SETS_;   // converter sets: set c converts the stages with st % SETS == c
-  static constexpr int kMmaWarps = MMAS_;   // MMA warps: warp m issues the stages with st % MMAS == m (a
+  static constexpr int kConvSets = SETS_;   // converter sets: set c converts groups j % SETS == c of a stage
+  static constexpr int kMmaWarps = MMAS_;   // MMA warps: warp m issues groups j % MMAS == m of a stage (a
                                             // thread stalls ~120 cycles per tcgen05.mma, so several
                                             // issuing warps keep the tensor core fed)
   static constexpr int kEpiWarps = EPIW_;   // 4 x column blocks x epilogue sets
-  static constexpr int kEpiSets = EPIS_;    // epilogue sets: set c promotes the stages with st % EPIS == c
+  static constexpr int kEpiSets = EPIS_;    // epilogue sets: set c promotes groups j % EPIS == c of a stage
   static constexpr int kEpiSetWarps = EPIW_ / EPIS_;  // warps of one epilogue set (4 x column blocks)
   static constexpr int kWarpConv0 = kWarpMma + kMmaWarps;
   static constexpr int kWarpEpi0 = kWarpConv0 + kConvSets * kConvWarps;
@@ -104,7 +104,7 @@ struct Cfg {
   static constexpr int kOffA = kOffWpk + STAGES * GPS * kWpkBytes;
   static constexpr int kOffSc = kOffA + (A_TMEM ? 0 : ABUF * GPS * kABytes);
   static constexpr int kOffBar = kOffSc + SSTAGES * kScBytes;
-  static constexpr int kNumBars = 2 * STAGES + 2 * TSTAGES + 2 * SSTAGES + 2 * ABUF + NP + 4;
+  static constexpr int kNumBars = 2 * STAGES + 2 * TSTAGES + 2 * SSTAGES + 2 * ABUF + 2 * NP + 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffSched = kOffMisc + 64;
   static constexpr int kSmemBytesMax = kOffSched + 2 * (kMaxExperts + 1) * 4 + 1024;
@@ -124,12 +124,6 @@ struct Cfg {
   static_assert(EPIS_ == 1 || EPIS_ == 2, "one or two epilogue sets");
   static_assert(EPIW_ % (4 * EPIS_) == 0, "each epilogue set covers all four lane quarters");
   static_assert(kOffSched + 2 * 257 * 4 + 1024 <= 227 * 1024, "shared memory (256 experts)");
-  static_assert(NP <= ABUF, "an A-slot completion barrier must not run a phase ahead of the epilogue");
-  // Every barrier slot must be waited on by one warp (set) of each role, which then meets the
-  // slot's phases in order; a phase-parity wait is only unambiguous under that condition.
-  static_assert(STAGES % SETS_ == 0 && ABUF % SETS_ == 0 && NP % SETS_ == 0, "converter sets own whole slots");
-  static_assert(ABUF % MMAS_ == 0 && TSTAGES % MMAS_ == 0, "MMA warps own whole slots");
-  static_assert(SSTAGES % EPIS_ == 0 && ABUF % EPIS_ == 0 && NP % EPIS_ == 0, "epilogue sets own whole slots");
 };
 
 struct GemmParams {
@@ -285,9 +279,10 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
   uint64_t* tempty = tfull + TSTAGES;
   uint64_t* sfull = tempty + TSTAGES;   // scale ring
   uint64_t* sempty = sfull + SSTAGES;
-  uint64_t* mready = sempty + SSTAGES;  // [ABUF] converted weights (and their P buffer) ready for the MMA
-  uint64_t* mdone = mready + ABUF;      // [ABUF] MMAs of the group done: A buffer free, partials ready
-  uint64_t* pempty = mdone + ABUF;      // [NP] partial buffer read by the epilogue
+  uint64_t* mready = sempty + SSTAGES;  // [ABUF] converted weights of a stage ready for the MMAs
+  uint64_t* mdone = mready + ABUF;      // [ABUF] MMAs of the stage done: A slot free
+  uint64_t* pfull = mdone + ABUF;       // [NP] MMAs of the stage done: partials ready
+  uint64_t* pempty = pfull + NP;        // [NP] partial slot read by the epilogue
   uint64_t* xfull = pempty + NP;        // [2] epilogue set 1 -> set 0 hand-over slot written
   uint64_t* xempty = xfull + 2;         // [2] hand-over slot read
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + CF::kOffMisc);
@@ -306,21 +301,24 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConvWarps);  // the 4 converter warps of the stage's set
+      mbar_init(&empty[s], kConvSets * kConvWarps);  // every converter warp
     }
     for (int s = 0; s < TSTAGES; ++s) {
       mbar_init(&tfull[s], 1);
-      mbar_init(&tempty[s], 1);  // the stage's MMA commit
+      mbar_init(&tempty[s], CF::kMmaWarps);  // one commit per MMA warp
     }
     for (int s = 0; s < SSTAGES; ++s) {
       mbar_init(&sfull[s], 1);
-      mbar_init(&sempty[s], CF::kEpiSetWarps);  // the warps of the stage's epilogue set
+      mbar_init(&sempty[s], CF::kEpiWarps);  // every epilogue warp
     }
     for (int b = 0; b < ABUF; ++b) {
-      mbar_init(&mready[b], kConvWarps);
-      mbar_init(&mdone[b], 1);
+      mbar_init(&mready[b], kConvSets * kConvWarps);
+      mbar_init(&mdone[b], CF::kMmaWarps);
     }
-    for (int b = 0; b < NP; ++b) mbar_init(&pempty[b], CF::kEpiSetWarps);
+    for (int b = 0; b < NP; ++b) {
+      mbar_init(&pfull[b], CF::kMmaWarps);
+      mbar_init(&pempty[b], CF::kEpiWarps);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&xfull[b], CF::kEpiSetWarps);
       mbar_init(&xempty[b], CF::kEpiSetWarps);
@@ -423,7 +421,7 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
       }
     }
   } else if (warp < kWarpConv0) {
-    // ---- MMA issue: warp m issues the stages with st % kMmaWarps == m ----
+    // ---- MMA issue: every stage; warp m issues the groups j with j % kMmaWarps == m ----
     const int mset = warp - kWarpMma;
     if (lane == 0) {
       uint32_t st = 0;
@@ -433,18 +431,22 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
         const int ncol = (row0 - (row0 & ~3) + rows + 15) & ~15;
         const uint32_t idesc = idesc_e4m3(static_cast<uint32_t>(ncol));
         for (int g0 = 0; g0 < G; g0 += gps, ++st) {
-          if (static_cast<int>(st % CF::kMmaWarps) != mset) continue;
           const int ts_ = st % TSTAGES;
           const uint32_t tph = (st / TSTAGES) & 1;
           const int a = st % ABUF;
           const uint32_t aph = (st / ABUF) & 1;
           const int pslot = st % NP;
-          // token tiles landed; weights converted (and their partial slot free)
-          if (!wait_bar(&tfull[ts_], tph, s_abort) || !wait_bar(&mready[a], aph, s_abort)) goto done;
+          const uint32_t pph = (st / NP) & 1;
+          // token tiles landed, weights converted, partial slot read by the epilogue
+          const bool ok = mbar_test3(&tfull[ts_], tph, &mready[a], aph, &pempty[pslot], pph ^ 1) ||
+                          (wait_bar(&tfull[ts_], tph, s_abort) && wait_bar(&mready[a], aph, s_abort) &&
+                           wait_bar(&pempty[pslot], pph ^ 1, s_abort));
+          if (!ok) goto done;
           tc_fence_after();
 #pragma unroll
           for (int j = 0; j < GPS; ++j) {
             if (j >= gps) break;
+            if (j % CF::kMmaWarps != mset) continue;
             const uint32_t d = tmem_base + (pslot * GPS + j) * NMAX;
             const uint32_t tok = smem_u32(s_tok + (ts_ * GPS + j) * CF::kTokBytes);
 #pragma unroll
@@ -459,34 +461,34 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
               }
             }
           }
-          mma_commit(&tempty[ts_]);
+          // a commit arrives once this thread's earlier MMAs are complete (at once if it issued none)
+          mma_commit(&pfull[pslot]);
           mma_commit(&mdone[a]);
+          mma_commit(&tempty[ts_]);
         }
       }
     }
   } else if (warp < kWarpEpi0) {
-    // ---- converters: int4 -> E4M3; set `cset` converts the stages with st % kConvSets == cset ----
+    // ---- converters: every stage; set c converts the groups j with j % kConvSets == c ----
     const int q4 = warp & 3;
     const int cset = (warp - kWarpConv0) / kConvWarps;
     const int r = q4 * 32 + lane;
     uint32_t st = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
       for (int g0 = 0; g0 < G; g0 += gps, ++st) {
-        if (static_cast<int>(st % kConvSets) != cset) continue;
         const int s = st % STAGES;
         const uint32_t ph = (st / STAGES) & 1;
         const int a = st % ABUF;
         const uint32_t aph = (st / ABUF) & 1;
-        const int pslot = st % NP;
-        const uint32_t pph = (st / NP) & 1;
-        // weights landed, the A slot's previous MMAs done, the partial slot read by the epilogue
-        const bool ok = mbar_test3(&full[s], ph, &mdone[a], aph ^ 1, &pempty[pslot], pph ^ 1) ||
-                        (wait_bar(&full[s], ph, s_abort) && wait_bar(&mdone[a], aph ^ 1, s_abort) &&
-                         wait_bar(&pempty[pslot], pph ^ 1, s_abort));
+        // weights landed; the A slot's previous MMAs done
+        bool ok = true;
+        if (!mbar_try_wait(&full[s], ph) || !mbar_try_wait(&mdone[a], aph ^ 1))
+          ok = wait_bar(&full[s], ph, s_abort) && wait_bar(&mdone[a], aph ^ 1, s_abort);
         if (__any_sync(0xffffffffu, !ok)) goto done;  // warp-uniform; the warp is converged below
 #pragma unroll
         for (int j = 0; j < GPS; ++j) {
           if (j >= gps) break;
+          if (j % kConvSets != cset) continue;
           const uint8_t* wrow = s_wpk + (s * GPS + j) * CF::kWpkBytes + r * 64;
           uint32_t in[16];
 #pragma unroll
@@ -511,7 +513,7 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);  // every packed byte of the stage is in registers by now
+        if (lane == 0) mbar_arrive(&empty[s]);  // every packed byte this warp reads is in registers by now
         if constexpr (CF::A_TMEM) {
           tmem_wait_st();
           tc_fence_before();
@@ -524,8 +526,8 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
     }
   } else {
     // ---- promotion and epilogue ----
-    // Warp w: lane quarter q4 = w & 3, epilogue set `eset` (the stages with st % EPIS == eset)
-    // and, within the set, column block `half`.
+    // Warp w: lane quarter q4 = w & 3, epilogue set `eset` (the groups j of every stage with
+    // j % EPIS == eset) and, within the set, column block `half`.
     const int ew = warp - kWarpEpi0;
     const int q4 = warp & 3;
     const int eset = ew / CF::kEpiSetWarps;
@@ -545,21 +547,22 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
 #pragma unroll
       for (int q = 0; q < NHALF / 2; ++q) acc2[q] = 0ull;
       for (int g0 = 0; g0 < G; g0 += gps, ++st) {
-        if (EPIS > 1 && static_cast<int>(st % EPIS) != eset) continue;
         const int ss = st % SSTAGES;
         const uint32_t sph = (st / SSTAGES) & 1;
-        const int a = st % ABUF;
-        const uint32_t aph = (st / ABUF) & 1;
         const int pslot = st % NP;
+        const uint32_t pph = (st / NP) & 1;
         const float* tsc = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes);
         const float* tcr = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes + CF::kTscBytes);
         const float* wsc = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes + 2 * CF::kTscBytes);
-        const bool ok = wait_bar(&sfull[ss], sph, s_abort) && wait_bar(&mdone[a], aph, s_abort);
+        bool ok = true;
+        if (!mbar_try_wait(&sfull[ss], sph) || !mbar_try_wait(&pfull[pslot], pph))
+          ok = wait_bar(&sfull[ss], sph, s_abort) && wait_bar(&pfull[pslot], pph, s_abort);
         if (__any_sync(0xffffffffu, !ok)) goto done;  // warp converged below
         tc_fence_after();
 #pragma unroll
         for (int j = 0; j < GPS; ++j) {
           if (j >= gps) break;
+          if (EPIS > 1 && j % EPIS != eset) continue;
           const float ws = wsc[j * kBM + r];
           uint64_t ws2;
           asm("mov.b64 %0, {%1, %1};" : "=l"(ws2) : "f"(ws));
@@ -767,7 +770,7 @@ int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, c
 }
 
 // decode: few rows per expert, weight streaming; converted weights in tensor memory
-using CfgDecode = Cfg<16, 2, 10, 8, 12, 4, 4, true, 2, 2, 4, 1>;
+using CfgDecode = Cfg<16, 4, 5, 4, 6, 2, 3, true, 2, 2, 4, 1>;
 // prefill: 128-row token tiles, one group per stage; converted weights in tensor memory
 using CfgPrefill = Cfg<128, 1, 8, 6, 8, 4, 2, true, 1, 2, 8, 1>;
 
