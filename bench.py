@@ -21,6 +21,7 @@ import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 if "--impl" in sys.argv and "reference" in sys.argv:
@@ -94,7 +95,7 @@ class ClockSampler:
     def __init__(self, uuid):
         self.uuid = uuid
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"w4a8moe_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:

@@ -20,8 +20,11 @@ the precision the method computes its scales in, so that codes are exact.
 Rounding of the bf16 tensors on the path (Y13, Y2, the layer output) is done
 once, from float64, to nearest even.
 
-Readings of points the pages leave open (quantisation formula, int4 nibble
-order, gate/up row order, top-k tie-break, ...) are listed in the design doc.
+Where the pages leave a point open, the plainest reading is taken and stated at
+the function that depends on it: s = amax/448 per token per 128 columns with
+amax clamped to >= 1e-12; int4 element 2b in the low nibble of byte b; w13 rows
+[0, I) gate, [I, 2I) up; top-k ties broken towards the lower expert index;
+softmax over the logits, then the top-k weights renormalised to sum to 1.
 
 Parity pins: see tests/test_oracle_*.py (exhaustive E4M3 codec, closed forms,
 brute force on tiny inputs, dense dequantise-then-matmul, integer special
