@@ -103,3 +103,30 @@ def test_linear(lib, M, N, K):
     err = rel_fro(got, ref)
     assert err <= 1e-3, (err, np.abs(got - ref).max())
     assert lib.device_error() == 0
+
+
+# Shapes with fewer 128-row weight tiles than SMs: K is split and a second kernel sums the
+# fp32 partials (decode tiles for M <= 32, 128-row tiles above).
+@pytest.mark.parametrize("M,N,K", [(1, 1024, 8192), (13, 512, 4096), (40, 256, 16384), (130, 256, 32768)])
+def test_linear_split_k(lib, M, N, K):
+    assert lib.linear_workspace_bytes(M, N, K) > 0
+    rng = np.random.default_rng(M * 11 + N + K)
+    aq, a_s = _acts(rng, M, K)
+    packed, ws = _weights(rng, 1, N, K)
+    got = f64_of_bf16(lib.w4a8_linear(to_dev(aq), scales_to_gpu_layout(a_s), scales_to_gpu_layout(gcorr_of(aq, a_s)),
+                                      prepacked(lib, packed[0]), to_dev(ws[0])))
+    ref = oracle.linear(aq, a_s, oracle.unpack_int4(packed[0]), ws[0].T)
+    err = rel_fro(got, ref)
+    assert err <= 1e-3, (err, np.abs(got - ref).max())
+    assert lib.device_error() == 0
+
+
+def test_linear_split_k_needs_workspace(lib):
+    M, N, K = 1, 1024, 8192
+    rng = np.random.default_rng(5)
+    aq, a_s = _acts(rng, M, K)
+    packed, ws = _weights(rng, 1, N, K)
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(lib.W4A8Error):
+        lib.w4a8_linear(to_dev(aq), scales_to_gpu_layout(a_s), scales_to_gpu_layout(gcorr_of(aq, a_s)),
+                        prepacked(lib, packed[0]), to_dev(ws[0]), ws=small)

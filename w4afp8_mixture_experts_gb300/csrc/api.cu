@@ -108,12 +108,8 @@ extern "C" int w4a8_device_error(void) {
 }
 
 extern "C" size_t w4a8_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int64_t E) {
-  (void)op;
-  (void)M;
-  (void)N;
-  (void)K;
   (void)E;
-  return 0;
+  return op == W4A8_OP_LINEAR ? w4a8::linear_workspace_bytes(M, N, K) : 0;
 }
 
 extern "C" int w4a8_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, int k,

@@ -24,6 +24,8 @@ int check_launch(const char* what);
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int num_sms();
+// split-K partial-sum bytes w4a8_linear needs for this shape on the current device (0: none)
+size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 // Device error word: bit 0 = a bounded mbarrier wait timed out, bit 1 = an
 // expert id was out of range.  Each translation unit that can raise one

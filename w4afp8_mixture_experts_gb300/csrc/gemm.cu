@@ -38,8 +38,9 @@
 //     its warps, so each barrier's waiters meet its phases in order: the
 //     condition under which a phase-parity wait cannot be satisfied by a stale
 //     phase.
-//   * Tiles: (expert, token chunk, 128-row weight block); chunks split an
-//     expert's rows evenly into pieces of at most NMAX; the schedule is built
+//   * Tiles: (expert, token chunk, 128-row weight block); chunks cut an
+//     expert's rows on a grid of NMAX rows that starts at its first row rounded
+//     down to a multiple of 4 (so scale vectors stay 16-byte aligned); the schedule is built
 //     in shared memory from seg_indptr by every CTA (no host synchronisation,
 //     no workspace), and CTAs stride over it.
 #include <algorithm>
@@ -116,7 +117,6 @@ struct Cfg {
   static constexpr int kXColBase = (kAColBase + (A_TMEM ? ABUF * GPS * 32 : 0) + 31) / 32 * 32;
   static constexpr int kTmemUsed = kXColBase + (EPIS_ > 1 ? 2 * NMAX : 0);
   static constexpr uint32_t kTmemCols = pow2_at_least(kTmemUsed);
-  static constexpr int kChunkMax = NMAX - 3;              // rows of a chunk (tile starts 4-aligned)
   static_assert(NMAX % 16 == 0 && NMAX >= 16 && NMAX <= 256, "token tile");
   static_assert(kTokBytes % 1024 == 0 && kOffWpk % 1024 == 0 && kOffA % 1024 == 0, "alignment");
   static_assert(kOffSc % 128 == 0 && kScBytes % 128 == 0, "TMA destinations 128-byte aligned");
@@ -129,8 +129,10 @@ struct Cfg {
 struct GemmParams {
   const int64_t* seg;  // [E+1] or nullptr (dense: one expert with M rows)
   uint16_t* C;
+  float* partial;      // split-K: fp32 partial sums [splits][M][N] instead of C (nullptr: write C)
   int E, N, K, M;      // M: rows of A (dense) / M_total
   int gps;             // 128-K groups per stage (divides K/128, <= Cfg::GPS)
+  int splits;          // K splits per tile (1: none)
 };
 
 // UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -185,7 +187,15 @@ struct Sched {
   const int* prefix;  // [E+1] chunk prefix
   const int* start;   // [E+1] row starts
   int E, NMAX, nblk;
-  __device__ __forceinline__ void decode(int item, int& e, int& nb, int& row0, int& rows) const {
+  int S, Gs, gps;     // K splits per tile, stages per tile, groups per stage
+  // item = tile * S + split; split s covers stages [s*Gs/S, (s+1)*Gs/S) of the tile
+  __device__ __forceinline__ void krange(int item, int& g_beg, int& g_end) const {
+    const int sp = item % S;
+    g_beg = (sp * Gs / S) * gps;
+    g_end = ((sp + 1) * Gs / S) * gps;
+  }
+  __device__ __forceinline__ void decode(int item_, int& e, int& nb, int& row0, int& rows) const {
+    const int item = item_ / S;
     const int chunk = item / nblk;
     nb = item - chunk * nblk;
     int lo = 0, hi = E;  // prefix[lo] <= chunk < prefix[hi]
@@ -194,13 +204,12 @@ struct Sched {
       if (prefix[mid] <= chunk) lo = mid; else hi = mid;
     }
     e = lo;
-    const int nc = prefix[e + 1] - prefix[e];
-    const int cnt = start[e + 1] - start[e];
-    const int cs = (cnt + nc - 1) / nc;
-    const int c = chunk - prefix[e];
-    const int r0 = c * cs;
-    row0 = start[e] + r0;
-    rows = min(cs, cnt - r0);
+    // chunks sit on a grid of NMAX rows from the expert's first row rounded down to 4, so a
+    // tile's token rows start 4-aligned (16-byte scale vectors) and only the first one is ragged
+    const int st = start[e], end = start[e + 1];
+    const int base = (st & ~3) + (chunk - prefix[e]) * NMAX;
+    row0 = max(st, base);
+    rows = min(end, base + NMAX) - row0;
   }
 };
 
@@ -247,7 +256,7 @@ __device__ __forceinline__ void promote2(uint64_t& acc2, uint64_t ws2, float t0,
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2) : "l"(ws2), "l"(e));
 }
 
-template <class CF>
+template <class CF, bool SPLIT>
 __global__ void __launch_bounds__(CF::kThreads, 1)
     w4a8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAS,
                      const __grid_constant__ CUtensorMap tmAC, const __grid_constant__ CUtensorMap tmB,
@@ -353,7 +362,7 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
         }
         s_start[e] = st;
       }
-      int v = (cnt + CF::kChunkMax - 1) / CF::kChunkMax;
+      int v = cnt > 0 ? ((st & 3) + cnt + NMAX - 1) / NMAX : 0;  // chunks on the NMAX-row grid
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int u = __shfl_up_sync(0xffffffffu, v, o);
@@ -369,8 +378,9 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
   tc_fence_after();
 
   const uint32_t tmem_base = *s_tmem;
-  Sched sch{s_prefix, s_start, E, NMAX, nblk};
-  const int n_items = s_prefix[E] * nblk;
+  const int S = SPLIT ? prm.splits : 1;  // 1 folds the split arithmetic away
+  Sched sch{s_prefix, s_start, E, NMAX, nblk, S, G / gps, gps};
+  const int n_items = s_prefix[E] * nblk * S;
 
   // Counters: `it` counts 128-K groups, `st` counts stages of gps groups; stage st holds
   // groups [st*gps, st*gps + gps) of one tile (gps divides K/128, so stages never straddle
@@ -384,7 +394,9 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
       for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
         int e, nb, row0, rows;
         sch.decode(item, e, nb, row0, rows);
-        for (int g0 = 0; g0 < G; g0 += gps, ++st) {
+        int g_beg, g_end;
+        sch.krange(item, g_beg, g_end);
+        for (int g0 = g_beg; g0 < g_end; g0 += gps, ++st) {
           const int s = st % STAGES;
           const uint32_t ph = (st / STAGES) & 1;
           if (!wait_bar(&empty[s], ph ^ 1, s_abort)) goto done;
@@ -403,7 +415,9 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
         int e, nb, row0, rows;
         sch.decode(item, e, nb, row0, rows);
         const int r4 = row0 & ~3;
-        for (int g0 = 0; g0 < G; g0 += gps, ++st) {
+        int g_beg, g_end;
+        sch.krange(item, g_beg, g_end);
+        for (int g0 = g_beg; g0 < g_end; g0 += gps, ++st) {
           const int ts_ = st % TSTAGES;
           const uint32_t tph = (st / TSTAGES) & 1;
           const int ss = st % SSTAGES;
@@ -430,7 +444,9 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
         sch.decode(item, e, nb, row0, rows);
         const int ncol = (row0 - (row0 & ~3) + rows + 15) & ~15;
         const uint32_t idesc = idesc_e4m3(static_cast<uint32_t>(ncol));
-        for (int g0 = 0; g0 < G; g0 += gps, ++st) {
+        int g_beg, g_end;
+        sch.krange(item, g_beg, g_end);
+        for (int g0 = g_beg; g0 < g_end; g0 += gps, ++st) {
           const int ts_ = st % TSTAGES;
           const uint32_t tph = (st / TSTAGES) & 1;
           const int a = st % ABUF;
@@ -475,7 +491,9 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
     const int r = q4 * 32 + lane;
     uint32_t st = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-      for (int g0 = 0; g0 < G; g0 += gps, ++st) {
+      int g_beg, g_end;
+      sch.krange(item, g_beg, g_end);
+      for (int g0 = g_beg; g0 < g_end; g0 += gps, ++st) {
         const int s = st % STAGES;
         const uint32_t ph = (st / STAGES) & 1;
         const int a = st % ABUF;
@@ -546,7 +564,9 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
       uint64_t acc2[NHALF / 2];   // packed pairs of fp32 accumulators
 #pragma unroll
       for (int q = 0; q < NHALF / 2; ++q) acc2[q] = 0ull;
-      for (int g0 = 0; g0 < G; g0 += gps, ++st) {
+      int g_beg, g_end;
+      sch.krange(item, g_beg, g_end);
+      for (int g0 = g_beg; g0 < g_end; g0 += gps, ++st) {
         const int ss = st % SSTAGES;
         const uint32_t sph = (st / SSTAGES) & 1;
         const int pslot = st % NP;
@@ -630,6 +650,18 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&xempty[xs]);
+      }
+      if (SPLIT) {  // split-K: fp32 partial sums of this split, reduced by a second kernel
+        float* prow = prm.partial + (static_cast<int64_t>(item % sch.S) * prm.M + r4) * prm.N + nb * kBM + r;
+#pragma unroll
+        for (int q = 0; q < NHALF / 2; ++q) {
+          float a0, a1;
+          asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc2[q]));
+          const int t = c0 + 2 * q;
+          if (t >= lo && t < lo + rows) prow[static_cast<int64_t>(t) * prm.N] = a0;
+          if (t + 1 >= lo && t + 1 < lo + rows) prow[static_cast<int64_t>(t + 1) * prm.N] = a1;
+        }
+        continue;
       }
       uint16_t* crow = prm.C + static_cast<int64_t>(r4) * prm.N + nb * kBM + r;
 #pragma unroll
@@ -716,12 +748,42 @@ struct Registrar {
   Registrar() { register_device_error_reader(&read_gemm_error); }
 } registrar;
 
+// groups per stage: the largest power of two <= Cfg::GPS dividing K/128
+template <class CF>
+int stage_groups(int64_t K) {
+  const int64_t G = K / kGroup;
+  int gps = 1;
+  while (gps * 2 <= CF::GPS && G % (gps * 2) == 0) gps *= 2;
+  return gps;
+}
+
+// K splits of a dense GEMM whose tiles leave SMs idle.  A CTA takes ceil(items / SMs) items of
+// ceil(stages / S) stages each, so the launch lasts about that many stage times; a split adds the
+// partial-sum pass (about two stage times) and may write at most a quarter of the weight bytes in
+// fp32 partials.  S = 1 .. 16 minimising that estimate, ties to the smaller S.
+template <class CF>
+int plan_splits(int64_t M, int64_t N, int64_t K, int sms) {
+  const int64_t tiles = ceil_div(M, CF::NMAX) * (N / kBM);
+  if (M <= 0 || tiles <= 0 || tiles >= sms) return 1;
+  const int64_t stages = K / kGroup / stage_groups<CF>(K);
+  int best = 1;
+  int64_t best_cost = ceil_div(tiles, sms) * stages;
+  for (int S = 2; S <= 16 && S <= stages && S * M * N * 4 <= N * K / 8; ++S) {
+    const int64_t cost = ceil_div(tiles * S, sms) * ceil_div(stages, S) + 2;
+    if (cost < best_cost) {
+      best = S;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
 template <class CF>
 int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, const uint8_t* B, const float* b_s,
-           const int64_t* seg, int64_t E, int64_t N, int64_t K, int64_t M, uint16_t* C, cudaStream_t st) {
+           const int64_t* seg, int64_t E, int64_t N, int64_t K, int64_t M, uint16_t* C, float* partial, int splits,
+           cudaStream_t st) {
   const int64_t G = K / kGroup;
-  int gps = 1;  // groups per stage: the largest power of two <= Cfg::GPS dividing K/128
-  while (gps * 2 <= CF::GPS && G % (gps * 2) == 0) gps *= 2;
+  const int gps = stage_groups<CF>(K);
   CUtensorMap tA, tAS, tAC, tB, tBS;
   int rc;
   {  // tokens viewed as [group][row][128 B]: one box = gps groups x NMAX rows
@@ -751,7 +813,9 @@ int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, c
     return rc;
   static bool attr_set = false;  // per template instance
   if (!attr_set) {
-    if (cudaFuncSetAttribute(w4a8_gemm_kernel<CF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(w4a8_gemm_kernel<CF, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             CF::kSmemBytesMax) != cudaSuccess ||
+        cudaFuncSetAttribute(w4a8_gemm_kernel<CF, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              CF::kSmemBytesMax) != cudaSuccess)
       return check_launch("cudaFuncSetAttribute(gemm)");
     attr_set = true;
@@ -764,8 +828,14 @@ int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, c
   p.K = static_cast<int>(K);
   p.M = static_cast<int>(M);
   p.gps = gps;
-  w4a8_gemm_kernel<CF><<<num_sms(), CF::kThreads, CF::smem_bytes(static_cast<int>(seg ? E : 1)), st>>>(
-      tA, tAS, tAC, tB, tBS, p);
+  p.partial = partial;
+  p.splits = splits;
+  if (splits > 1)
+    w4a8_gemm_kernel<CF, true><<<num_sms(), CF::kThreads, CF::smem_bytes(static_cast<int>(seg ? E : 1)), st>>>(
+        tA, tAS, tAC, tB, tBS, p);
+  else
+    w4a8_gemm_kernel<CF, false><<<num_sms(), CF::kThreads, CF::smem_bytes(static_cast<int>(seg ? E : 1)), st>>>(
+        tA, tAS, tAC, tB, tBS, p);
   return check_launch("w4a8_gemm_kernel");
 }
 
@@ -774,8 +844,35 @@ using CfgDecode = Cfg<16, 4, 5, 4, 6, 2, 3, true, 2, 2, 4, 1>;
 // prefill: 128-row token tiles, one group per stage; converted weights in tensor memory
 using CfgPrefill = Cfg<128, 1, 8, 6, 8, 4, 2, true, 1, 2, 8, 1>;
 
+// C[m][n] = bf16(sum over s of partial[s][m][n]), four columns per thread.
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ partial,
+                                                            uint16_t* __restrict__ C, int64_t MN, int S) {
+  for (int64_t i = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) * 4; i < MN;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x * 4) {
+    float4 acc = *reinterpret_cast<const float4*>(partial + i);
+    for (int s = 1; s < S; ++s) {
+      const float4 v = *reinterpret_cast<const float4*>(partial + s * MN + i);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    uint2 o;
+    o.x = static_cast<uint32_t>(float_to_bf16_bits(acc.x)) | (static_cast<uint32_t>(float_to_bf16_bits(acc.y)) << 16);
+    o.y = static_cast<uint32_t>(float_to_bf16_bits(acc.z)) | (static_cast<uint32_t>(float_to_bf16_bits(acc.w)) << 16);
+    *reinterpret_cast<uint2*>(C + i) = o;
+  }
+}
+
+// K splits the dense Linear uses for this shape on the current device (1: none).
+int linear_splits(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0 || N % kBM || K % kGroup) return 1;
+  return M <= 32 ? plan_splits<CfgDecode>(M, N, K, num_sms()) : plan_splits<CfgPrefill>(M, N, K, num_sms());
+}
+
 int gemm_common(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, const uint8_t* B, const float* b_s,
-                const int64_t* seg, int64_t E, int64_t N, int64_t K, int64_t M, uint16_t* C, void* stream) {
+                const int64_t* seg, int64_t E, int64_t N, int64_t K, int64_t M, uint16_t* C, void* ws,
+                size_t ws_bytes, void* stream) {
   W4A8_REQUIRE(K > 0 && K % kGroup == 0, "K=%lld must be a positive multiple of 128", (long long)K);
   W4A8_REQUIRE(N > 0 && N % kBM == 0, "N=%lld must be a positive multiple of 128", (long long)N);
   W4A8_REQUIRE(M >= 0 && M < (1ll << 31), "M=%lld out of range", (long long)M);
@@ -788,32 +885,51 @@ int gemm_common(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_
                "device pointers must be 16-byte aligned");
   if (M == 0) return W4A8_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // split-K only for the dense GEMM: the grouped GEMM's tile count depends on device-side seg_indptr
+  const int S = seg ? 1 : linear_splits(M, N, K);
+  float* partial = nullptr;
+  if (S > 1) {
+    const size_t need = static_cast<size_t>(S) * M * N * sizeof(float);
+    W4A8_REQUIRE(ws != nullptr && ws_bytes >= need && aligned16(ws),
+                 "workspace of %zu bytes (16-byte aligned) required for this shape, got %zu", need, ws_bytes);
+    partial = static_cast<float*>(ws);
+  }
+  int rc;
   // Few rows per expert: weight streaming, 16-wide token tiles and a deep ring.
   if (M <= 32 * E)
-    return launch<CfgDecode>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, st);
-  return launch<CfgPrefill>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, st);
+    rc = launch<CfgDecode>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st);
+  else
+    rc = launch<CfgPrefill>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st);
+  if (rc != W4A8_OK || S == 1) return rc;
+  const int64_t MN = M * N;  // N % 128 == 0, so MN % 4 == 0
+  const int64_t blocks = ceil_div(MN / 4, 256) < 8 * 152 ? ceil_div(MN / 4, 256) : 8 * 152;
+  splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(partial, C, MN, S);
+  return check_launch("splitk_reduce_kernel");
 }
 
 }  // namespace
+
+size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const int S = linear_splits(M, N, K);
+  return S > 1 ? static_cast<size_t>(S) * M * N * sizeof(float) : 0;
+}
+
 }  // namespace w4a8
 
 extern "C" int w4a8_grouped_gemm(const uint8_t* A, const float* a_scales, const float* a_gcorr, int64_t a_scale_ld,
                                  const uint8_t* B_prepacked, const float* b_scales, const int64_t* seg_indptr,
                                  int64_t E, int64_t N, int64_t K, int64_t M_total, uint16_t* C, void* ws,
                                  size_t ws_bytes, void* stream) {
-  (void)ws;
-  (void)ws_bytes;
   W4A8_REQUIRE(seg_indptr != nullptr, "seg_indptr is null");
   return w4a8::gemm_common(A, a_scales, a_gcorr, a_scale_ld, B_prepacked, b_scales, seg_indptr, E, N, K, M_total, C,
-                           stream);
+                           ws, ws_bytes, stream);
 }
 
 extern "C" int w4a8_linear(const uint8_t* A, const float* a_scales, const float* a_gcorr, int64_t a_scale_ld,
                            const uint8_t* B_prepacked, const float* b_scales, int64_t M, int64_t N, int64_t K,
                            uint16_t* C, void* ws, size_t ws_bytes, void* stream) {
-  (void)ws;
-  (void)ws_bytes;
-  return w4a8::gemm_common(A, a_scales, a_gcorr, a_scale_ld, B_prepacked, b_scales, nullptr, 1, N, K, M, C, stream);
+  return w4a8::gemm_common(A, a_scales, a_gcorr, a_scale_ld, B_prepacked, b_scales, nullptr, 1, N, K, M, C, ws,
+                           ws_bytes, stream);
 }
 
 extern "C" int w4a8_prepack_weights(const uint8_t* w, int64_t rows, int64_t K, uint8_t* out, void* stream) {
