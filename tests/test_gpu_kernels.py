@@ -84,6 +84,10 @@ def _bf16_rows(rng, M, K):
         x[2, 5] = 3.0e4                         # a spike
     if M > 4:
         x[4, :] = np.float32(1e-30)             # tiny values
+    if M > 6:
+        x[5, 7] = 3.0e38                        # near the bf16 maximum: scale ~7e35
+        x[6, 0::2] = -0.0                       # signed zeros: codes 0x80 / 0x00
+        x[6, 1::2] = 0.0
     return inputs.to_bf16_bits(x)
 
 

@@ -1,11 +1,13 @@
 // FP8 E4M3 quantisation per token per 128-column group, and SiLU-and-Mul with
 // re-quantisation of the intermediate.
 //
-// One warp per (row, group): each lane owns 4 consecutive values (one 8-byte
-// load per operand), the group's amax is a shuffle max, the scale amax/448 and
-// the quotients x/s are IEEE fp32 divisions, and the codes come from the
-// hardware cvt.rn.satfinite.e4m3x2 (round to nearest even, saturate to +-448,
-// as on the PR #37796 page's fp8 write path).  The amax clamp to 1e-12 follows
+// Activations: one thread per (row, group) keeps the group's 128 values in
+// registers (amax pass, then quantisation pass).  SiLU-and-Mul: one warp per
+// (row, group), each lane owning 4 consecutive values, amax by shuffles.  The
+// scale amax/448 is an IEEE fp32 division; the quotients x/s are the correctly
+// rounded fp32 quotients; the codes come from the hardware
+// cvt.rn.satfinite.e4m3x2 (round to nearest even, saturate to +-448, as on the
+// PR #37796 page's fp8 write path).  The amax clamp to 1e-12 follows
 // the DeepGEMM PR #53 page (padded rows would give 448/0).
 #include <cuda_fp16.h>
 
@@ -28,6 +30,24 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {  // exact: E4M3 -> 
   return __half2float(__ushort_as_half(static_cast<uint16_t>(h2 & 0xFFFFu)));
 }
 
+// x / s rounded to nearest even in fp32 from r = RN(1/s), by Markstein's correction step
+// (P. Markstein, "Computation of elementary functions on the IBM RISC System/6000 processor",
+// IBM J. Res. Dev. 34(1), 1990): if r is within half an ulp of 1/s and q within one ulp of x/s,
+// the residual e = x - q*s is exact in one fma and RN(q + e*r) is the correctly rounded
+// quotient.  RN(x*r) can be two ulps off (relative error up to 2^-23), so one correction first
+// brings it within an ulp and a second one rounds correctly.  Valid while nothing overflows or
+// underflows; quotients below 2^-10 all quantise to a signed E4M3 zero whatever their last
+// bits, so tiny x is harmless.
+// The steps need s and r = 1/s normal: amax >= 1e-12 keeps s >= 2.2e-15, and a finite amax keeps
+// r >= 2^-120; an infinite or NaN amax (r = 0 or NaN) takes the IEEE division instead.
+__device__ __forceinline__ float div_by_scale(float x, float s, float r) {
+  if (!(r > 0.0f && r < INFINITY)) return __fdiv_rn(x, s);
+  const float q0 = __fmul_rn(x, r);
+  const float q1 = __fmaf_rn(__fmaf_rn(-q0, s, x), r, q0);
+  // the sum of the correction can turn -0 into +0; the quotient's sign is x's (s > 0)
+  return copysignf(__fmaf_rn(__fmaf_rn(-q1, s, x), r, q1), x);
+}
+
 // Quantise 4 values of one 128-group held by this lane; writes the codes and (lane 0) the
 // scale and the group's correction term of the symmetric weight encoding:
 //   gcorr = -1/2 * s * sum_k e4m3(code_k)  (lane sums, then a fixed xor-tree over lanes).
@@ -37,8 +57,9 @@ __device__ __forceinline__ void quant_group4(float f0, float f1, float f2, float
   amax = warp_max(amax);
   amax = fmaxf(amax, 1e-12f);
   const float s = __fdiv_rn(amax, 448.0f);
-  const uint32_t lo = e4m3x2(__fdiv_rn(f0, s), __fdiv_rn(f1, s));
-  const uint32_t hi = e4m3x2(__fdiv_rn(f2, s), __fdiv_rn(f3, s));
+  const float r = __frcp_rn(s);
+  const uint32_t lo = e4m3x2(div_by_scale(f0, s, r), div_by_scale(f1, s, r));
+  const uint32_t hi = e4m3x2(div_by_scale(f2, s, r), div_by_scale(f3, s, r));
   const uint32_t codes = lo | (hi << 16);
   *reinterpret_cast<uint32_t*>(qdst + lane * 4) = codes;
   if (cdst) {
@@ -51,24 +72,64 @@ __device__ __forceinline__ void quant_group4(float f0, float f1, float f2, float
   if (lane == 0) *sdst = s;
 }
 
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
-    quant_kernel(const uint16_t* __restrict__ x, int64_t K, const int32_t* __restrict__ row_index,
-                 int64_t row_div, int64_t M_out, uint8_t* __restrict__ q, float* __restrict__ scales,
-                 float* __restrict__ gcorr, int64_t ld) {
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// One thread per (row, 128-group): the group's 256 bytes stay in registers between the amax
+// pass and the quantisation pass, so no cross-lane reduction is needed.  amax is taken on the
+// bf16 magnitude bits (same order as the values for non-NaN inputs).
+__global__ void __launch_bounds__(128)
+    quant_lane_kernel(const uint16_t* __restrict__ x, int64_t K, const int32_t* __restrict__ row_index,
+                      int64_t row_div, int64_t M_out, uint8_t* __restrict__ q, float* __restrict__ scales,
+                      float* __restrict__ gcorr, int64_t ld) {
   const int64_t G = K / kGroup;
-  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int64_t row = gw / G;
-  if (row >= M_out) return;
-  const int64_t g = gw - row * G;
+  const int64_t task = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (task >= M_out * G) return;
+  const int64_t row = task / G;
+  const int64_t g = task - row * G;
   const int64_t src = row_index ? static_cast<int64_t>(row_index[row]) / row_div : row;
-  const uint2 raw = *reinterpret_cast<const uint2*>(x + src * K + g * kGroup + lane * 4);
-  const float f0 = __uint_as_float(raw.x << 16);
-  const float f1 = __uint_as_float(raw.x & 0xFFFF0000u);
-  const float f2 = __uint_as_float(raw.y << 16);
-  const float f3 = __uint_as_float(raw.y & 0xFFFF0000u);
-  quant_group4(f0, f1, f2, f3, lane, q + row * K + g * kGroup, scales + g * ld + row,
-               gcorr ? gcorr + g * ld + row : nullptr);
+  const uint4* xp = reinterpret_cast<const uint4*>(x + src * K + g * kGroup);
+  uint32_t w[64];
+  uint32_t mx = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint4 v = __ldg(xp + i);
+    w[4 * i + 0] = v.x;
+    w[4 * i + 1] = v.y;
+    w[4 * i + 2] = v.z;
+    w[4 * i + 3] = v.w;
+    mx = __vmaxu2(mx, __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu));
+    mx = __vmaxu2(mx, __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+  }
+  mx = max(mx & 0xFFFFu, mx >> 16);
+  const float amax = fmaxf(__uint_as_float(mx << 16), 1e-12f);
+  const float s = __fdiv_rn(amax, 448.0f);
+  const float r = __frcp_rn(s);
+  uint8_t* qp = q + row * K + g * kGroup;
+  float sum = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    uint32_t c[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t v = w[4 * i + j];
+      c[j] = e4m3x2(div_by_scale(bf16_lo(v), s, r), div_by_scale(bf16_hi(v), s, r));
+    }
+    const uint32_t c01 = c[0] | (c[1] << 16), c23 = c[2] | (c[3] << 16);
+    if (gcorr) {
+      // E4M3 pairs -> f16 pairs (exact) -> fp32 partial sums
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t h2;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(c[j])));
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+        sum += f.x + f.y;
+      }
+    }
+    reinterpret_cast<uint2*>(qp)[i] = make_uint2(c01, c23);  // the 8 codes of this 16-byte chunk
+  }
+  scales[g * ld + row] = s;
+  if (gcorr) gcorr[g * ld + row] = -0.5f * __fmul_rn(s, sum);
 }
 
 // h = silu(gate) * up = gate / (1 + exp(-gate)) * up, fp32.
@@ -110,15 +171,15 @@ extern "C" int fp8_quant_per_token_group(const uint16_t* x, int64_t M_src, int64
   W4A8_REQUIRE(scale_ld >= M_out && scale_ld % 4 == 0, "scale_ld must be >= M_out and a multiple of 4");
   if (M_out == 0) return W4A8_OK;
   W4A8_REQUIRE(x && q && scales, "null pointer");
-  W4A8_REQUIRE(((uintptr_t)x & 7) == 0 && ((uintptr_t)q & 3) == 0 && ((uintptr_t)scales & 3) == 0 &&
+  W4A8_REQUIRE(((uintptr_t)x & 15) == 0 && ((uintptr_t)q & 7) == 0 && ((uintptr_t)scales & 3) == 0 &&
                    ((uintptr_t)gcorr & 3) == 0,
-               "x must be 8-byte and q, scales, gcorr 4-byte aligned");
-  const int64_t warps = M_out * (K / kGroup);
-  const int64_t blocks = ceil_div(warps, kWarpsPerBlock);
+               "x must be 16-byte, q 8-byte and scales, gcorr 4-byte aligned");
+  const int64_t tasks = M_out * (K / kGroup);
+  const int64_t blocks = ceil_div(tasks, 128);
   W4A8_REQUIRE(blocks < (1ll << 31), "too many rows");
-  quant_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, static_cast<cudaStream_t>(stream)>>>(
+  quant_lane_kernel<<<static_cast<unsigned>(blocks), 128, 0, static_cast<cudaStream_t>(stream)>>>(
       x, K, row_index, row_div, M_out, q, scales, gcorr, scale_ld);
-  return check_launch("quant_kernel");
+  return check_launch("quant_lane_kernel");
 }
 
 extern "C" int silu_mul_requant(const uint16_t* gate_up, int64_t M, int64_t I, uint8_t* q, float* scales,
