@@ -508,21 +508,38 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
           if (j >= gps) break;
           if (j % kConvSets != cset) continue;
           const uint8_t* wrow = s_wpk + (s * GPS + j) * CF::kWpkBytes + r * 64;
-          uint32_t in[16];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((q ^ ((r >> 1) & 3)) << 4));
-            in[4 * q + 0] = v.x;
-            in[4 * q + 1] = v.y;
-            in[4 * q + 2] = v.z;
-            in[4 * q + 3] = v.w;
-          }
-          uint32_t out[32];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) int4x8_to_e4m3x8(in[i], out[2 * i], out[2 * i + 1]);
           if constexpr (CF::A_TMEM) {
-            tmem_st32(tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + CF::kAColBase + (a * GPS + j) * 32, out);
+            // two halves of 64 weights: 8 packed words -> 16 E4M3 words -> 16 tensor-memory columns
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t in[8];
+#pragma unroll
+              for (int q = 0; q < 2; ++q) {
+                const uint4 v = *reinterpret_cast<const uint4*>(wrow + (((2 * hh + q) ^ ((r >> 1) & 3)) << 4));
+                in[4 * q + 0] = v.x;
+                in[4 * q + 1] = v.y;
+                in[4 * q + 2] = v.z;
+                in[4 * q + 3] = v.w;
+              }
+              uint32_t out[16];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) int4x8_to_e4m3x8(in[i], out[2 * i], out[2 * i + 1]);
+              tmem_st16(tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + CF::kAColBase + (a * GPS + j) * 32 + 16 * hh,
+                        out);
+            }
           } else {
+            uint32_t in[16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((q ^ ((r >> 1) & 3)) << 4));
+              in[4 * q + 0] = v.x;
+              in[4 * q + 1] = v.y;
+              in[4 * q + 2] = v.z;
+              in[4 * q + 3] = v.w;
+            }
+            uint32_t out[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) int4x8_to_e4m3x8(in[i], out[2 * i], out[2 * i + 1]);
             uint8_t* arow = s_a + (a * GPS + j) * CF::kABytes + r * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c)
