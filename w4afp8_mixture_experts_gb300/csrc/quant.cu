@@ -1,7 +1,7 @@
 // FP8 E4M3 quantisation per token per 128-column group, and SiLU-and-Mul with
 // re-quantisation of the intermediate.
 //
-// Activations: one thread per (row, group) keeps the group's 128 values in
+// Activations: four lanes per (row, group) keep the group's 128 values in
 // registers (amax pass, then quantisation pass).  SiLU-and-Mul: one warp per
 // (row, group), each lane owning 4 consecutive values, amax by shuffles.  The
 // scale amax/448 is an IEEE fp32 division; the quotients x/s are the correctly
@@ -75,24 +75,31 @@ __device__ __forceinline__ void quant_group4(float f0, float f1, float f2, float
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// One thread per (row, 128-group): the group's 256 bytes stay in registers between the amax
-// pass and the quantisation pass, so no cross-lane reduction is needed.  amax is taken on the
-// bf16 magnitude bits (same order as the values for non-NaN inputs).
-__global__ void __launch_bounds__(128)
-    quant_lane_kernel(const uint16_t* __restrict__ x, int64_t K, const int32_t* __restrict__ row_index,
+// Four consecutive lanes per (row, 128-group), 32 values each: the values stay in registers
+// between the amax pass and the quantisation pass, and the group's amax and code sum take two
+// shuffle steps.  amax is taken on the bf16 magnitude bits (same order as the values for non-NaN
+// inputs).
+constexpr int kQuantLanes = 4;                     // lanes per group
+constexpr int kQuantVals = kGroup / kQuantLanes;   // values per lane
+
+__global__ void __launch_bounds__(256)
+    quant_quad_kernel(const uint16_t* __restrict__ x, int64_t K, const int32_t* __restrict__ row_index,
                       int64_t row_div, int64_t M_out, uint8_t* __restrict__ q, float* __restrict__ scales,
                       float* __restrict__ gcorr, int64_t ld) {
   const int64_t G = K / kGroup;
-  const int64_t task = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t task = tid / kQuantLanes;
+  const int sub = static_cast<int>(tid % kQuantLanes);
+  // whole quads leave together (M_out * G * 4 threads are launched rounded up to the block)
   if (task >= M_out * G) return;
   const int64_t row = task / G;
   const int64_t g = task - row * G;
   const int64_t src = row_index ? static_cast<int64_t>(row_index[row]) / row_div : row;
-  const uint4* xp = reinterpret_cast<const uint4*>(x + src * K + g * kGroup);
-  uint32_t w[64];
+  const uint4* xp = reinterpret_cast<const uint4*>(x + src * K + g * kGroup + sub * kQuantVals);
+  uint32_t w[kQuantVals / 2];
   uint32_t mx = 0;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
+  for (int i = 0; i < kQuantVals / 8; ++i) {
     const uint4 v = __ldg(xp + i);
     w[4 * i + 0] = v.x;
     w[4 * i + 1] = v.y;
@@ -102,20 +109,22 @@ __global__ void __launch_bounds__(128)
     mx = __vmaxu2(mx, __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
   }
   mx = max(mx & 0xFFFFu, mx >> 16);
+  const unsigned quad = 0xFu << (threadIdx.x & 28);  // the four lanes of this group
+  mx = max(mx, __shfl_xor_sync(quad, mx, 1));
+  mx = max(mx, __shfl_xor_sync(quad, mx, 2));
   const float amax = fmaxf(__uint_as_float(mx << 16), 1e-12f);
   const float s = __fdiv_rn(amax, 448.0f);
   const float r = __frcp_rn(s);
-  uint8_t* qp = q + row * K + g * kGroup;
+  uint8_t* qp = q + row * K + g * kGroup + sub * kQuantVals;
   float sum = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
+  for (int i = 0; i < kQuantVals / 8; ++i) {
     uint32_t c[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const uint32_t v = w[4 * i + j];
       c[j] = e4m3x2(div_by_scale(bf16_lo(v), s, r), div_by_scale(bf16_hi(v), s, r));
     }
-    const uint32_t c01 = c[0] | (c[1] << 16), c23 = c[2] | (c[3] << 16);
     if (gcorr) {
       // E4M3 pairs -> f16 pairs (exact) -> fp32 partial sums
 #pragma unroll
@@ -126,10 +135,16 @@ __global__ void __launch_bounds__(128)
         sum += f.x + f.y;
       }
     }
-    reinterpret_cast<uint2*>(qp)[i] = make_uint2(c01, c23);  // the 8 codes of this 16-byte chunk
+    reinterpret_cast<uint2*>(qp)[i] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
   }
-  scales[g * ld + row] = s;
-  if (gcorr) gcorr[g * ld + row] = -0.5f * __fmul_rn(s, sum);
+  if (gcorr) {
+    sum += __shfl_xor_sync(quad, sum, 1);
+    sum += __shfl_xor_sync(quad, sum, 2);
+  }
+  if (sub == 0) {
+    scales[g * ld + row] = s;
+    if (gcorr) gcorr[g * ld + row] = -0.5f * __fmul_rn(s, sum);
+  }
 }
 
 // h = silu(gate) * up = gate / (1 + exp(-gate)) * up, fp32.
@@ -174,12 +189,12 @@ extern "C" int fp8_quant_per_token_group(const uint16_t* x, int64_t M_src, int64
   W4A8_REQUIRE(((uintptr_t)x & 15) == 0 && ((uintptr_t)q & 7) == 0 && ((uintptr_t)scales & 3) == 0 &&
                    ((uintptr_t)gcorr & 3) == 0,
                "x must be 16-byte, q 8-byte and scales, gcorr 4-byte aligned");
-  const int64_t tasks = M_out * (K / kGroup);
-  const int64_t blocks = ceil_div(tasks, 128);
+  const int64_t threads = M_out * (K / kGroup) * kQuantLanes;
+  const int64_t blocks = ceil_div(threads, 256);
   W4A8_REQUIRE(blocks < (1ll << 31), "too many rows");
-  quant_lane_kernel<<<static_cast<unsigned>(blocks), 128, 0, static_cast<cudaStream_t>(stream)>>>(
+  quant_quad_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
       x, K, row_index, row_div, M_out, q, scales, gcorr, scale_ld);
-  return check_launch("quant_lane_kernel");
+  return check_launch("quant_quad_kernel");
 }
 
 extern "C" int silu_mul_requant(const uint16_t* gate_up, int64_t M, int64_t I, uint8_t* q, float* scales,
