@@ -220,7 +220,8 @@ class MoeRunner:
         b = self.ws.data_ptr()
         L = self.L
         self.p = {n: b + getattr(L, n) for n in ("topk_ids", "topk_w", "seg_indptr", "src2dst", "dst2src",
-                                                 "xq", "xs", "xc", "y13", "hq", "hs", "hc", "y2")}
+                                                 "xq", "xs", "xc", "y13", "hq", "hs", "hc", "y2", "permute_ws")}
+        self.permute_ws_bytes = int(m.load().w4a8_workspace_bytes(1, T * k, 0, 0, E))
         self.ld = L.scale_ld
 
     def stages(self, stream):
@@ -232,7 +233,7 @@ class MoeRunner:
         return [
             ("route", lambda: lib.moe_route_topk(lg, T, E, k, 1, p["topk_ids"], p["topk_w"], stream)),
             ("permute", lambda: lib.moe_permute(p["topk_ids"], T, k, E, p["seg_indptr"], p["src2dst"],
-                                                p["dst2src"], None, 0, stream)),
+                                                p["dst2src"], p["permute_ws"], self.permute_ws_bytes, stream)),
             ("quant", lambda: lib.fp8_quant_per_token_group(x, T, H, p["dst2src"], k, P, p["xq"], p["xs"], p["xc"],
                                                             ld, stream)),
             ("w13", lambda: lib.w4a8_grouped_gemm(p["xq"], p["xs"], p["xc"], ld, w13, w13s, p["seg_indptr"], E,

@@ -162,6 +162,7 @@ int w4a8_prepack_weights(const uint8_t* w, int64_t rows, int64_t K, uint8_t* out
  * the quantisation of (3) on h.
  *   gate_up bf16 [M][2I]   q uint8 [M][I]   scales, gcorr fp32 [I/128][scale_ld]
  *   I % 128 == 0, scale_ld >= M, scale_ld % 4 == 0.  gcorr may be NULL.
+ *   gate_up 16-byte aligned, q 8-byte aligned, scales and gcorr 4-byte aligned.
  */
 int silu_mul_requant(const uint16_t* gate_up, int64_t M, int64_t I, uint8_t* q, float* scales,
                      float* gcorr, int64_t scale_ld, void* stream);

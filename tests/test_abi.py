@@ -51,6 +51,7 @@ P16 = ctypes.c_void_p(16)  # a 16-byte aligned non-null dummy (never dereference
     (lambda L: L.moe_route_topk(P16, 4, 8, 9, 1, P16, P16, NULL), b"k=9"),
     (lambda L: L.moe_route_topk(P16, 4, 2000, 2, 1, P16, P16, NULL), b"E=2000"),
     (lambda L: L.moe_permute(P16, 4, 2, 0, P16, P16, P16, NULL, 0, NULL), b"E=0"),
+    (lambda L: L.moe_permute(P16, 1024, 8, 256, P16, P16, P16, NULL, 0, NULL), b"workspace"),
     (lambda L: L.fp8_quant_per_token_group(P16, 4, 100, NULL, 1, 4, P16, P16, NULL, 4, NULL), b"K=100"),
     (lambda L: L.fp8_quant_per_token_group(P16, 4, 128, NULL, 1, 4, P16, P16, NULL, 2, NULL), b"scale_ld"),
     (lambda L: L.w4a8_grouped_gemm(P16, P16, P16, 4, P16, P16, P16, 2, 256, 200, 4, P16, NULL, 0, NULL), b"K=200"),

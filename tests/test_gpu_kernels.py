@@ -52,8 +52,10 @@ def _distinct_ids(rng, T, E, k, skew=None):
     return ids
 
 
+# from 8192 pairs the permutation runs over several CTAs (count pass + placement pass)
 @pytest.mark.parametrize("T,E,k", [(1, 1, 1), (5, 8, 2), (64, 256, 8), (1000, 384, 8), (4096, 16, 4),
-                                   (2049, 1024, 3)])
+                                   (2049, 1024, 3), (1024, 256, 8), (8192, 256, 8), (4096, 1024, 8),
+                                   (3001, 7, 3)])
 def test_permute(lib, T, E, k):
     rng = np.random.default_rng(T + E + k)
     ids = _distinct_ids(rng, T, E, k)
@@ -91,7 +93,8 @@ def _bf16_rows(rng, M, K):
     return inputs.to_bf16_bits(x)
 
 
-@pytest.mark.parametrize("M,K", [(1, 128), (37, 256), (300, 7168), (1024, 2048)])
+# 1200 x 7168 has more than 65536 groups: the four-lanes-per-group kernel (sixteen below that)
+@pytest.mark.parametrize("M,K", [(1, 128), (37, 256), (300, 7168), (1024, 2048), (1200, 7168)])
 def test_quant(lib, M, K):
     rng = np.random.default_rng(M + K)
     xb = _bf16_rows(rng, M, K)
@@ -124,7 +127,7 @@ def test_quant_gather(lib):
     assert np.array_equal(scales_from_gpu_layout(s, T * k), rs[tok])
 
 
-@pytest.mark.parametrize("M,I", [(3, 128), (77, 512), (512, 2048)])
+@pytest.mark.parametrize("M,I", [(3, 128), (77, 512), (512, 2048), (4200, 2048)])
 def test_silu_mul_requant(lib, M, I):
     # Codes are decided in fp32 on both sides, but exp differs in the last bit between the
     # device and numpy, so a code may move by one step on a rounding tie.

@@ -128,7 +128,9 @@ def moe_permute(topk_ids, E: int):
     seg = torch.empty(E + 1, dtype=torch.int64, device=dev)
     s2d = torch.empty(T * k, dtype=torch.int32, device=dev)
     d2s = torch.empty(T * k, dtype=torch.int32, device=dev)
-    _check(load().moe_permute(_p(topk_ids), T, k, E, _p(seg), _p(s2d), _p(d2s), None, 0, _stream()))
+    need = int(load().w4a8_workspace_bytes(1, T * k, 0, 0, E))
+    ws = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
+    _check(load().moe_permute(_p(topk_ids), T, k, E, _p(seg), _p(s2d), _p(d2s), _p(ws), need, _stream()))
     return seg, s2d, d2s
 
 

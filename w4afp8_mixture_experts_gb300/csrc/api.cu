@@ -75,7 +75,7 @@ int layout_of(int64_t T, int64_t H, int64_t I, int64_t E, int k, w4a8_moe_layout
   L->hs = take((I / 128) * ld * 4);
   L->hc = take((I / 128) * ld * 4);
   L->y2 = take(P * H * 2);
-  L->permute_ws = take(0);
+  L->permute_ws = take(permute_ws_bytes(P, E));
   L->scale_ld = ld;
   L->total = o;
   return W4A8_OK;
@@ -109,7 +109,9 @@ extern "C" int w4a8_device_error(void) {
 
 extern "C" size_t w4a8_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int64_t E) {
   (void)E;
-  return op == W4A8_OP_LINEAR ? w4a8::linear_workspace_bytes(M, N, K) : 0;
+  if (op == W4A8_OP_LINEAR) return w4a8::linear_workspace_bytes(M, N, K);
+  if (op == W4A8_OP_PERMUTE) return w4a8::permute_ws_bytes(M, E);
+  return 0;
 }
 
 extern "C" int w4a8_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, int k,
@@ -150,7 +152,7 @@ extern "C" int w4a8_moe_forward(const uint16_t* x, const float* logits, int64_t 
   uint16_t* y2 = reinterpret_cast<uint16_t*>(b + L.y2);
   const int64_t P = T * k;
   if ((rc = moe_route_topk(logits, T, E, k, renormalize, ids, tw, stream))) return rc;
-  if ((rc = moe_permute(ids, T, k, E, seg, s2d, d2s, nullptr, 0, stream))) return rc;
+  if ((rc = moe_permute(ids, T, k, E, seg, s2d, d2s, b + L.permute_ws, permute_ws_bytes(P, E), stream))) return rc;
   if ((rc = fp8_quant_per_token_group(x, T, H, d2s, k, P, xq, xs, xc, L.scale_ld, stream))) return rc;
   if ((rc = w4a8_grouped_gemm(xq, xs, xc, L.scale_ld, w13, w13_s, seg, E, 2 * I, H, P, y13, nullptr, 0, stream)))
     return rc;

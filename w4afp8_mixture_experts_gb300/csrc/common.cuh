@@ -26,6 +26,8 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int num_sms();
 // split-K partial-sum bytes w4a8_linear needs for this shape on the current device (0: none)
 size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
+// per-chunk expert-count table moe_permute needs for P pairs (0: none)
+size_t permute_ws_bytes(int64_t P, int64_t E);
 
 // Device error word: bit 0 = a bounded mbarrier wait timed out, bit 1 = an
 // expert id was out of range.  Each translation unit that can raise one

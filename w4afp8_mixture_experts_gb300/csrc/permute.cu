@@ -3,47 +3,31 @@
 // seg_indptr[E+1] int64, src2dst int32).  No sort is needed: a counting sort
 // gives the same order.
 //
-// One CTA of 1024 threads: a shared-memory histogram, an exclusive scan into
-// seg_indptr, then the pairs in chunks of 1024 in flat order.  Inside a chunk,
-// a pair's rank among the chunk's earlier pairs of the same expert is its rank
-// inside its warp (__match_any_sync) plus the counts of the lower warps, which
-// one pass over a [32][E] table of per-warp counts turns into prefixes.
+// Up to 8191 pairs: one CTA of 1024 threads builds a shared-memory histogram,
+// scans it into seg_indptr and places the pairs.  From 8192 pairs: the pairs are
+// cut into CTA chunks; pass 1 counts each chunk's experts into a workspace table,
+// pass 2 derives every chunk's first position per expert from that table and
+// places the chunk's pairs the same way.
 #include "common.cuh"
 
 namespace w4a8 {
 namespace {
 
 constexpr int kThreads = 1024;
+constexpr int kMultiMin = 8192;  // pairs from which the work is spread over several CTAs
 __device__ unsigned int g_permute_error;
 
-__global__ void __launch_bounds__(kThreads, 1)
-    permute_kernel(const int32_t* __restrict__ ids, int P, int E, int64_t* __restrict__ seg,
-                   int32_t* __restrict__ src2dst, int32_t* __restrict__ dst2src) {
-  extern __shared__ int sm[];
-  int* run = sm;           // [E] counts, then running start of each expert
-  int* wh = sm + E;        // [32][E] per-warp counts of the current chunk
-  __shared__ int warp_tot[32];
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
+// Pairs per CTA of the multi-CTA path: a multiple of 1024, at least 2048, at most 1024 CTAs.
+__host__ __device__ inline int64_t permute_chunk(int64_t P) {
+  int64_t c = (P + 1023) / 1024;
+  c = (c + 1023) / 1024 * 1024;
+  return c < 2048 ? 2048 : c;
+}
 
-  for (int i = tid; i < E; i += kThreads) run[i] = 0;
-  for (int i = tid; i < 32 * E; i += kThreads) wh[i] = 0;
-  __syncthreads();
-  bool bad = false;
-  for (int f = tid; f < P; f += kThreads) {
-    const int e = ids[f];
-    if (e < 0 || e >= E) {
-      bad = true;
-      continue;
-    }
-    atomicAdd(&run[e], 1);
-  }
-  if (bad) atomicOr(&g_permute_error, 2u);
-  __syncthreads();
-
-  // exclusive scan of run[0..E) (E <= 1024: one value per thread)
-  const int c = tid < E ? run[tid] : 0;
+// Block-wide exclusive scan of v (one value per thread, E <= 1024 entries); returns the exclusive
+// prefix and the total in *tot.
+__device__ __forceinline__ int block_excl_scan(int c, int* warp_tot, int* tot) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int v = c;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -60,21 +44,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane >= o) t += u;
     }
     warp_tot[lane] = t - warp_tot[lane];  // exclusive
+    if (lane == 31) warp_tot[32] = t;     // grand total
   }
   __syncthreads();
   const int excl = v - c + warp_tot[warp];
-  if (tid < E) {
-    run[tid] = excl;
-    seg[tid] = excl;
-  }
-  if (tid == E - 1) seg[E] = excl + c;
-  __syncthreads();
+  *tot = warp_tot[32];
+  return excl;
+}
 
+// Sorted positions of the pairs [f0, f1) given run[e] = first free position of expert e: chunks of
+// 1024 in flat order; inside a chunk a pair's rank among the chunk's earlier pairs of its expert is
+// its rank inside its warp (__match_any_sync) plus the counts of the lower warps, which one pass
+// over a [32][E] table of per-warp counts turns into prefixes.
+__device__ void place_pairs(const int32_t* __restrict__ ids, int f0, int f1, int E, int* run, int* wh,
+                            int32_t* __restrict__ src2dst, int32_t* __restrict__ dst2src) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const unsigned lt = (1u << lane) - 1u;
-  for (int base = 0; base < P; base += kThreads) {
+  for (int base = f0; base < f1; base += kThreads) {
     const int f = base + tid;
     int e = -1;
-    if (f < P) {
+    if (f < f1) {
       e = ids[f];
       if (e < 0 || e >= E) e = -1;
     }
@@ -104,6 +93,95 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// One CTA: histogram, scan into seg_indptr, placement.
+__global__ void __launch_bounds__(kThreads, 1)
+    permute_kernel(const int32_t* __restrict__ ids, int P, int E, int64_t* __restrict__ seg,
+                   int32_t* __restrict__ src2dst, int32_t* __restrict__ dst2src) {
+  extern __shared__ int sm[];
+  int* run = sm;           // [E] counts, then running start of each expert
+  int* wh = sm + E;        // [32][E] per-warp counts of the current chunk
+  __shared__ int warp_tot[33];
+  const int tid = threadIdx.x;
+
+  for (int i = tid; i < E; i += kThreads) run[i] = 0;
+  for (int i = tid; i < 32 * E; i += kThreads) wh[i] = 0;
+  __syncthreads();
+  bool bad = false;
+  for (int f = tid; f < P; f += kThreads) {
+    const int e = ids[f];
+    if (e < 0 || e >= E) {
+      bad = true;
+      continue;
+    }
+    atomicAdd(&run[e], 1);
+  }
+  if (bad) atomicOr(&g_permute_error, 2u);
+  __syncthreads();
+  const int c = tid < E ? run[tid] : 0;
+  int tot;
+  const int excl = block_excl_scan(c, warp_tot, &tot);
+  if (tid < E) {
+    run[tid] = excl;
+    seg[tid] = excl;
+  }
+  if (tid == 0) seg[E] = tot;
+  __syncthreads();
+  place_pairs(ids, 0, P, E, run, wh, src2dst, dst2src);
+}
+
+// Several CTAs, pass 1: CTA b counts the experts of pairs [b*C, (b+1)*C) into cnt[b][E].
+__global__ void __launch_bounds__(kThreads)
+    permute_count_kernel(const int32_t* __restrict__ ids, int P, int E, int C, int* __restrict__ cnt) {
+  extern __shared__ int hist[];
+  const int tid = threadIdx.x;
+  for (int i = tid; i < E; i += kThreads) hist[i] = 0;
+  __syncthreads();
+  const int f0 = blockIdx.x * C, f1 = min(P, f0 + C);
+  bool bad = false;
+  for (int f = f0 + tid; f < f1; f += kThreads) {
+    const int e = ids[f];
+    if (e < 0 || e >= E) {
+      bad = true;
+      continue;
+    }
+    atomicAdd(&hist[e], 1);
+  }
+  if (bad) atomicOr(&g_permute_error, 2u);
+  __syncthreads();
+  for (int i = tid; i < E; i += kThreads) cnt[static_cast<int64_t>(blockIdx.x) * E + i] = hist[i];
+}
+
+// Pass 2: CTA b derives expert e's first position for its pairs (all pairs of lower experts, plus
+// expert e's pairs in lower CTAs), CTA 0 writes seg_indptr, then places its pairs.
+__global__ void __launch_bounds__(kThreads, 1)
+    permute_place_kernel(const int32_t* __restrict__ ids, int P, int E, int C, const int* __restrict__ cnt,
+                         int64_t* __restrict__ seg, int32_t* __restrict__ src2dst, int32_t* __restrict__ dst2src) {
+  extern __shared__ int sm[];
+  int* run = sm;
+  int* wh = sm + E;
+  __shared__ int warp_tot[33];
+  const int tid = threadIdx.x;
+  for (int i = tid; i < 32 * E; i += kThreads) wh[i] = 0;
+  int total = 0, before = 0;
+  if (tid < E) {
+    for (int b = 0; b < static_cast<int>(gridDim.x); ++b) {
+      const int v = cnt[static_cast<int64_t>(b) * E + tid];
+      if (b < static_cast<int>(blockIdx.x)) before += v;
+      total += v;
+    }
+  }
+  int tot;
+  const int excl = block_excl_scan(tid < E ? total : 0, warp_tot, &tot);
+  if (tid < E) run[tid] = excl + before;
+  if (blockIdx.x == 0) {
+    if (tid < E) seg[tid] = excl;
+    if (tid == 0) seg[E] = tot;
+  }
+  __syncthreads();
+  const int f0 = blockIdx.x * C;
+  place_pairs(ids, f0, min(P, f0 + C), E, run, wh, src2dst, dst2src);
+}
+
 int read_permute_error() {
   unsigned int v = 0;
   cudaMemcpyFromSymbol(&v, g_permute_error, sizeof(v));
@@ -119,24 +197,51 @@ struct Registrar {
 }  // namespace
 }  // namespace w4a8
 
+namespace w4a8 {
+
+size_t permute_ws_bytes(int64_t P, int64_t E) {
+  if (P < kMultiMin || E < 1) return 0;
+  const int64_t blocks = (P + permute_chunk(P) - 1) / permute_chunk(P);
+  return static_cast<size_t>(blocks * E) * sizeof(int);
+}
+
+}  // namespace w4a8
+
 extern "C" int moe_permute(const int32_t* topk_ids, int64_t T, int k, int64_t E, int64_t* seg_indptr,
                            int32_t* src2dst, int32_t* dst2src, void* ws, size_t ws_bytes, void* stream) {
   using namespace w4a8;
-  (void)ws;
-  (void)ws_bytes;
   W4A8_REQUIRE(T >= 0 && k >= 1 && T * k < (1ll << 31), "T*k out of range");
   W4A8_REQUIRE(E >= 1 && E <= 1024, "E=%lld must be in [1, 1024]", (long long)E);
   W4A8_REQUIRE(seg_indptr != nullptr, "seg_indptr is null");
   W4A8_REQUIRE(T == 0 || (topk_ids && src2dst && dst2src), "null pointer");
+  const int64_t P = T * k;
+  const size_t need = permute_ws_bytes(P, E);
+  W4A8_REQUIRE(need == 0 || (ws != nullptr && ws_bytes >= need && (reinterpret_cast<uintptr_t>(ws) & 3) == 0),
+               "workspace of %zu bytes (4-byte aligned) required for %lld pairs, got %zu", need, (long long)P,
+               ws_bytes);
   const size_t smem = static_cast<size_t>(33 * E) * sizeof(int);
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 33 * 1024 * 4) !=
-        cudaSuccess)
+            cudaSuccess ||
+        cudaFuncSetAttribute(permute_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 33 * 1024 * 4) !=
+            cudaSuccess)
       return check_launch("cudaFuncSetAttribute(permute)");
     attr_set = true;
   }
-  permute_kernel<<<1, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(
-      topk_ids, static_cast<int>(T * k), static_cast<int>(E), seg_indptr, src2dst, dst2src);
-  return check_launch("permute_kernel");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (need == 0) {
+    permute_kernel<<<1, kThreads, smem, st>>>(topk_ids, static_cast<int>(P), static_cast<int>(E), seg_indptr, src2dst,
+                                               dst2src);
+    return check_launch("permute_kernel");
+  }
+  const int C = static_cast<int>(permute_chunk(P));
+  const int blocks = static_cast<int>((P + C - 1) / C);
+  int* cnt = static_cast<int*>(ws);
+  permute_count_kernel<<<blocks, kThreads, static_cast<size_t>(E) * sizeof(int), st>>>(
+      topk_ids, static_cast<int>(P), static_cast<int>(E), C, cnt);
+  if (int rc = check_launch("permute_count_kernel")) return rc;
+  permute_place_kernel<<<blocks, kThreads, smem, st>>>(topk_ids, static_cast<int>(P), static_cast<int>(E), C, cnt,
+                                                       seg_indptr, src2dst, dst2src);
+  return check_launch("permute_place_kernel");
 }

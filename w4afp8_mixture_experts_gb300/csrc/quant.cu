@@ -1,9 +1,9 @@
 // FP8 E4M3 quantisation per token per 128-column group, and SiLU-and-Mul with
 // re-quantisation of the intermediate.
 //
-// Activations: four lanes per (row, group) keep the group's 128 values in
-// registers (amax pass, then quantisation pass).  SiLU-and-Mul: one warp per
-// (row, group), each lane owning 4 consecutive values, amax by shuffles.  The
+// 4 (large launches) or 16 (small ones) lanes per (row, group), whose values stay
+// in registers between the amax pass and the quantisation pass (the SiLU-and-Mul
+// kernel holds h).  The
 // scale amax/448 is an IEEE fp32 division; the quotients x/s are the correctly
 // rounded fp32 quotients; the codes come from the hardware
 // cvt.rn.satfinite.e4m3x2 (round to nearest even, saturate to +-448, as on the
@@ -15,20 +15,6 @@
 
 namespace w4a8 {
 namespace {
-
-constexpr int kWarpsPerBlock = 8;
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
-__device__ __forceinline__ float e4m3_value(uint32_t code) {  // exact: E4M3 -> f16 -> f32
-  uint32_t h2;  // the code in both bytes, so either half of the result holds its value
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(code | (code << 8))));
-  return __half2float(__ushort_as_half(static_cast<uint16_t>(h2 & 0xFFFFu)));
-}
 
 // x / s rounded to nearest even in fp32 from r = RN(1/s), by Markstein's correction step
 // (P. Markstein, "Computation of elementary functions on the IBM RISC System/6000 processor",
@@ -48,49 +34,27 @@ __device__ __forceinline__ float div_by_scale(float x, float s, float r) {
   return copysignf(__fmaf_rn(__fmaf_rn(-q1, s, x), r, q1), x);
 }
 
-// Quantise 4 values of one 128-group held by this lane; writes the codes and (lane 0) the
-// scale and the group's correction term of the symmetric weight encoding:
-//   gcorr = -1/2 * s * sum_k e4m3(code_k)  (lane sums, then a fixed xor-tree over lanes).
-__device__ __forceinline__ void quant_group4(float f0, float f1, float f2, float f3, int lane, uint8_t* qdst,
-                                             float* sdst, float* cdst) {
-  float amax = fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3)));
-  amax = warp_max(amax);
-  amax = fmaxf(amax, 1e-12f);
-  const float s = __fdiv_rn(amax, 448.0f);
-  const float r = __frcp_rn(s);
-  const uint32_t lo = e4m3x2(div_by_scale(f0, s, r), div_by_scale(f1, s, r));
-  const uint32_t hi = e4m3x2(div_by_scale(f2, s, r), div_by_scale(f3, s, r));
-  const uint32_t codes = lo | (hi << 16);
-  *reinterpret_cast<uint32_t*>(qdst + lane * 4) = codes;
-  if (cdst) {
-    float sum = (e4m3_value(codes & 0xFF) + e4m3_value((codes >> 8) & 0xFF)) +
-                (e4m3_value((codes >> 16) & 0xFF) + e4m3_value(codes >> 24));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) *cdst = -0.5f * __fmul_rn(s, sum);
-  }
-  if (lane == 0) *sdst = s;
-}
-
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Four consecutive lanes per (row, 128-group), 32 values each: the values stay in registers
-// between the amax pass and the quantisation pass, and the group's amax and code sum take two
-// shuffle steps.  amax is taken on the bf16 magnitude bits (same order as the values for non-NaN
+// LANES consecutive lanes per (row, 128-group), 128 / LANES values each: the values stay in
+// registers between the amax pass and the quantisation pass, and the group's amax and code sum
+// take log2(LANES) shuffle steps.  amax is taken on the bf16 magnitude bits (same order as the values for non-NaN
 // inputs).
-constexpr int kQuantLanes = 4;                     // lanes per group
-constexpr int kQuantVals = kGroup / kQuantLanes;   // values per lane
+// Lanes per group: 4 for large launches, 16 for small ones (more threads in flight).
+constexpr int kSmallLaunchGroups = 1 << 16;
 
+template <int LANES>
 __global__ void __launch_bounds__(256)
     quant_quad_kernel(const uint16_t* __restrict__ x, int64_t K, const int32_t* __restrict__ row_index,
                       int64_t row_div, int64_t M_out, uint8_t* __restrict__ q, float* __restrict__ scales,
                       float* __restrict__ gcorr, int64_t ld) {
+  constexpr int kQuantVals = kGroup / LANES;  // values per lane
   const int64_t G = K / kGroup;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t task = tid / kQuantLanes;
-  const int sub = static_cast<int>(tid % kQuantLanes);
-  // whole quads leave together (M_out * G * 4 threads are launched rounded up to the block)
+  const int64_t task = tid / LANES;
+  const int sub = static_cast<int>(tid % LANES);
+  // a group's lanes leave together (M_out * G * LANES threads are launched rounded up to the block)
   if (task >= M_out * G) return;
   const int64_t row = task / G;
   const int64_t g = task - row * G;
@@ -109,9 +73,9 @@ __global__ void __launch_bounds__(256)
     mx = __vmaxu2(mx, __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
   }
   mx = max(mx & 0xFFFFu, mx >> 16);
-  const unsigned quad = 0xFu << (threadIdx.x & 28);  // the four lanes of this group
-  mx = max(mx, __shfl_xor_sync(quad, mx, 1));
-  mx = max(mx, __shfl_xor_sync(quad, mx, 2));
+  const unsigned quad = ((1u << LANES) - 1u) << (threadIdx.x & (32 - LANES));  // this group's lanes
+#pragma unroll
+  for (int o = 1; o < LANES; o <<= 1) mx = max(mx, __shfl_xor_sync(quad, mx, o));
   const float amax = fmaxf(__uint_as_float(mx << 16), 1e-12f);
   const float s = __fdiv_rn(amax, 448.0f);
   const float r = __frcp_rn(s);
@@ -138,8 +102,8 @@ __global__ void __launch_bounds__(256)
     reinterpret_cast<uint2*>(qp)[i] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
   }
   if (gcorr) {
-    sum += __shfl_xor_sync(quad, sum, 1);
-    sum += __shfl_xor_sync(quad, sum, 2);
+#pragma unroll
+    for (int o = 1; o < LANES; o <<= 1) sum += __shfl_xor_sync(quad, sum, o);
   }
   if (sub == 0) {
     scales[g * ld + row] = s;
@@ -152,24 +116,70 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
 }
 
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
-    silu_mul_requant_kernel(const uint16_t* __restrict__ gu, int64_t M, int64_t I, uint8_t* __restrict__ q,
-                            float* __restrict__ scales, float* __restrict__ gcorr, int64_t ld) {
+// SiLU-and-Mul + requantisation, four lanes per (row, 128-group) as in quant_quad_kernel: each
+// lane computes its 32 values of h = silu(gate) * up into registers, then quantises them.
+template <int LANES>
+__global__ void __launch_bounds__(256)
+    silu_quad_kernel(const uint16_t* __restrict__ gu, int64_t M, int64_t I, uint8_t* __restrict__ q,
+                     float* __restrict__ scales, float* __restrict__ gcorr, int64_t ld) {
+  constexpr int kQuantVals = kGroup / LANES;  // values per lane
   const int64_t G = I / kGroup;
-  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int64_t row = gw / G;
-  if (row >= M) return;
-  const int64_t g = gw - row * G;
-  const uint16_t* base = gu + row * 2 * I + g * kGroup + lane * 4;
-  const uint2 gr = *reinterpret_cast<const uint2*>(base);
-  const uint2 ur = *reinterpret_cast<const uint2*>(base + I);
-  const float h0 = silu_mul(__uint_as_float(gr.x << 16), __uint_as_float(ur.x << 16));
-  const float h1 = silu_mul(__uint_as_float(gr.x & 0xFFFF0000u), __uint_as_float(ur.x & 0xFFFF0000u));
-  const float h2 = silu_mul(__uint_as_float(gr.y << 16), __uint_as_float(ur.y << 16));
-  const float h3 = silu_mul(__uint_as_float(gr.y & 0xFFFF0000u), __uint_as_float(ur.y & 0xFFFF0000u));
-  quant_group4(h0, h1, h2, h3, lane, q + row * I + g * kGroup, scales + g * ld + row,
-               gcorr ? gcorr + g * ld + row : nullptr);
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t task = tid / LANES;
+  const int sub = static_cast<int>(tid % LANES);
+  if (task >= M * G) return;  // a group's lanes leave together
+  const int64_t row = task / G;
+  const int64_t g = task - row * G;
+  const uint4* gp = reinterpret_cast<const uint4*>(gu + row * 2 * I + g * kGroup + sub * kQuantVals);
+  const uint4* up = reinterpret_cast<const uint4*>(gu + row * 2 * I + I + g * kGroup + sub * kQuantVals);
+  float h[kQuantVals];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kQuantVals / 8; ++i) {
+    const uint4 gv = __ldg(gp + i);
+    const uint4 uv = __ldg(up + i);
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      h[8 * i + 2 * j] = silu_mul(bf16_lo(gw[j]), bf16_lo(uw[j]));
+      h[8 * i + 2 * j + 1] = silu_mul(bf16_hi(gw[j]), bf16_hi(uw[j]));
+      amax = fmaxf(amax, fmaxf(fabsf(h[8 * i + 2 * j]), fabsf(h[8 * i + 2 * j + 1])));
+    }
+  }
+  const unsigned quad = ((1u << LANES) - 1u) << (threadIdx.x & (32 - LANES));
+#pragma unroll
+  for (int o = 1; o < LANES; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(quad, amax, o));
+  amax = fmaxf(amax, 1e-12f);
+  const float s = __fdiv_rn(amax, 448.0f);
+  const float r = __frcp_rn(s);
+  uint8_t* qp = q + row * I + g * kGroup + sub * kQuantVals;
+  float sum = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kQuantVals / 8; ++i) {
+    uint32_t c[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      c[j] = e4m3x2(div_by_scale(h[8 * i + 2 * j], s, r), div_by_scale(h[8 * i + 2 * j + 1], s, r));
+    if (gcorr) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t h2;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(c[j])));
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+        sum += f.x + f.y;
+      }
+    }
+    reinterpret_cast<uint2*>(qp)[i] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+  }
+  if (gcorr) {
+#pragma unroll
+    for (int o = 1; o < LANES; o <<= 1) sum += __shfl_xor_sync(quad, sum, o);
+  }
+  if (sub == 0) {
+    scales[g * ld + row] = s;
+    if (gcorr) gcorr[g * ld + row] = -0.5f * __fmul_rn(s, sum);
+  }
 }
 
 }  // namespace
@@ -189,11 +199,16 @@ extern "C" int fp8_quant_per_token_group(const uint16_t* x, int64_t M_src, int64
   W4A8_REQUIRE(((uintptr_t)x & 15) == 0 && ((uintptr_t)q & 7) == 0 && ((uintptr_t)scales & 3) == 0 &&
                    ((uintptr_t)gcorr & 3) == 0,
                "x must be 16-byte, q 8-byte and scales, gcorr 4-byte aligned");
-  const int64_t threads = M_out * (K / kGroup) * kQuantLanes;
-  const int64_t blocks = ceil_div(threads, 256);
+  const int64_t groups = M_out * (K / kGroup);
+  const bool small = groups < kSmallLaunchGroups;
+  const int64_t blocks = ceil_div(groups * (small ? 16 : 4), 256);
   W4A8_REQUIRE(blocks < (1ll << 31), "too many rows");
-  quant_quad_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      x, K, row_index, row_div, M_out, q, scales, gcorr, scale_ld);
+  if (small)
+    quant_quad_kernel<16><<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        x, K, row_index, row_div, M_out, q, scales, gcorr, scale_ld);
+  else
+    quant_quad_kernel<4><<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        x, K, row_index, row_div, M_out, q, scales, gcorr, scale_ld);
   return check_launch("quant_quad_kernel");
 }
 
@@ -205,12 +220,18 @@ extern "C" int silu_mul_requant(const uint16_t* gate_up, int64_t M, int64_t I, u
   W4A8_REQUIRE(scale_ld >= M && scale_ld % 4 == 0, "scale_ld must be >= M and a multiple of 4");
   if (M == 0) return W4A8_OK;
   W4A8_REQUIRE(gate_up && q && scales, "null pointer");
-  W4A8_REQUIRE(((uintptr_t)gate_up & 7) == 0 && ((uintptr_t)q & 3) == 0 && ((uintptr_t)scales & 3) == 0 &&
+  W4A8_REQUIRE(((uintptr_t)gate_up & 15) == 0 && ((uintptr_t)q & 7) == 0 && ((uintptr_t)scales & 3) == 0 &&
                    ((uintptr_t)gcorr & 3) == 0,
-               "gate_up must be 8-byte and q, scales, gcorr 4-byte aligned");
-  const int64_t blocks = ceil_div(M * (I / kGroup), kWarpsPerBlock);
+               "gate_up must be 16-byte, q 8-byte and scales, gcorr 4-byte aligned");
+  const int64_t groups = M * (I / kGroup);
+  const bool small = groups < kSmallLaunchGroups;
+  const int64_t blocks = ceil_div(groups * (small ? 16 : 4), 256);
   W4A8_REQUIRE(blocks < (1ll << 31), "too many rows");
-  silu_mul_requant_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0,
-                            static_cast<cudaStream_t>(stream)>>>(gate_up, M, I, q, scales, gcorr, scale_ld);
-  return check_launch("silu_mul_requant_kernel");
+  if (small)
+    silu_quad_kernel<16><<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        gate_up, M, I, q, scales, gcorr, scale_ld);
+  else
+    silu_quad_kernel<4><<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        gate_up, M, I, q, scales, gcorr, scale_ld);
+  return check_launch("silu_quad_kernel");
 }
