@@ -1,6 +1,7 @@
 // Unpermute and combine (SGLang PR #7762 page: post-reordering of the outputs):
 // out[t][c] = bf16( sum_j topk_w[t][j] * Y[src2dst[t*k+j]][c] ), fp32 in j order.
-// One CTA per token; 16-byte loads of 8 bf16 per thread and step.
+// CTA per token (and, for few tokens, per slice of 2048 columns); each thread loads the k rows' 8 bf16 of its
+// columns with 16-byte loads.
 #include "common.cuh"
 
 namespace w4a8 {
@@ -19,10 +20,12 @@ __global__ void __launch_bounds__(kThreads)
     ws[threadIdx.x] = w[t * k + threadIdx.x];
   }
   __syncthreads();
-  for (int64_t c = static_cast<int64_t>(threadIdx.x) * 8; c < H; c += kThreads * 8) {
+  for (int64_t c = (static_cast<int64_t>(blockIdx.y) * kThreads + threadIdx.x) * 8; c < H;
+       c += static_cast<int64_t>(gridDim.y) * kThreads * 8) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll 8
     for (int j = 0; j < k; ++j) {
       const uint4 v = *reinterpret_cast<const uint4*>(Y + rows[j] + c);
       const float wj = ws[j];
@@ -54,7 +57,9 @@ extern "C" int moe_unpermute_combine(const uint16_t* Y, const int32_t* src2dst, 
   if (T == 0) return W4A8_OK;
   W4A8_REQUIRE(Y && src2dst && topk_w && out, "null pointer");
   W4A8_REQUIRE(aligned16(Y) && aligned16(out), "Y and out must be 16-byte aligned");
-  combine_kernel<<<static_cast<unsigned>(T), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(Y, src2dst, topk_w,
-                                                                                              k, H, out);
+  // few tokens: also split the columns over CTAs, so that the SMs have work
+  const int64_t slices = T >= 2 * num_sms() ? 1 : ceil_div(H, kThreads * 8);
+  const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>(slices < 65535 ? slices : 65535));
+  combine_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(Y, src2dst, topk_w, k, H, out);
   return check_launch("combine_kernel");
 }
