@@ -14,6 +14,8 @@ __global__ void __launch_bounds__(kThreads)
                    int k, int64_t H, uint16_t* __restrict__ out) {
   __shared__ int64_t rows[32];
   __shared__ float ws[32];
+  pdl_trigger();
+  pdl_wait();
   const int64_t t = blockIdx.x;
   if (threadIdx.x < k) {
     rows[threadIdx.x] = static_cast<int64_t>(s2d[t * k + threadIdx.x]) * H;
@@ -60,6 +62,6 @@ extern "C" int moe_unpermute_combine(const uint16_t* Y, const int32_t* src2dst, 
   // few tokens: also split the columns over CTAs, so that the SMs have work
   const int64_t slices = T >= 2 * num_sms() ? 1 : ceil_div(H, kThreads * 8);
   const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>(slices < 65535 ? slices : 65535));
-  combine_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(Y, src2dst, topk_w, k, H, out);
-  return check_launch("combine_kernel");
+  return launch_pdl("combine_kernel", combine_kernel, grid, dim3(kThreads), 0, static_cast<cudaStream_t>(stream), Y,
+                    src2dst, topk_w, k, H, out);
 }

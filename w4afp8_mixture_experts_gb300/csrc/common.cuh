@@ -16,6 +16,25 @@ namespace w4a8 {
 int set_error(int status, const char* fmt, ...);
 int check_launch(const char* what);
 
+// Launch `kernel` with programmatic stream serialisation (see pdl_wait / pdl_trigger).
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(const char* what, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = st;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&lc, kernel, static_cast<KArgs>(args)...);
+  if (e != cudaSuccess) return set_error(W4A8_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return check_launch(what);
+}
+
 #define W4A8_REQUIRE(cond, ...)                                  \
   do {                                                           \
     if (!(cond)) return ::w4a8::set_error(W4A8_ERR_INVALID_ARG, __VA_ARGS__); \
@@ -122,6 +141,14 @@ __device__ __forceinline__ bool mbar_test3(uint64_t* a, uint32_t pa, uint64_t* b
       : "memory");
   return ok != 0;
 }
+
+// --- programmatic dependent launch -------------------------------------------
+// A kernel launched with launch_pdl may start while the previous kernel of the stream still runs:
+// it calls pdl_wait() before touching anything an earlier kernel writes, and pdl_trigger() lets the
+// next kernel launch once every CTA of this one has started.  Both are no-ops for a kernel launched
+// without the attribute (or after a non-kernel operation).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // --- TMA --------------------------------------------------------------------
 

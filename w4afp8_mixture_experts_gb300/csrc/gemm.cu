@@ -300,6 +300,7 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
   int* s_prefix = reinterpret_cast<int*>(smem + CF::kOffSched);  // [E+1]
   int* s_start = s_prefix + (E + 1);                              // [E+1]
 
+  pdl_trigger();  // the next kernel may launch once every CTA has started (it waits for this grid)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = prm.K / kGroup;
@@ -346,6 +347,8 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmBS);
   }
+  // everything above touched only this CTA's own state; inputs written by earlier kernels from here on
+  pdl_wait();
   if (warp == kWarpConv0) {  // chunk prefix over experts (warp-wide scan)
     int carry = 0;
     if (lane == 0) s_prefix[0] = 0;
@@ -847,13 +850,9 @@ int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, c
   p.gps = gps;
   p.partial = partial;
   p.splits = splits;
-  if (splits > 1)
-    w4a8_gemm_kernel<CF, true><<<num_sms(), CF::kThreads, CF::smem_bytes(static_cast<int>(seg ? E : 1)), st>>>(
-        tA, tAS, tAC, tB, tBS, p);
-  else
-    w4a8_gemm_kernel<CF, false><<<num_sms(), CF::kThreads, CF::smem_bytes(static_cast<int>(seg ? E : 1)), st>>>(
-        tA, tAS, tAC, tB, tBS, p);
-  return check_launch("w4a8_gemm_kernel");
+  return launch_pdl("w4a8_gemm_kernel", splits > 1 ? w4a8_gemm_kernel<CF, true> : w4a8_gemm_kernel<CF, false>,
+                    dim3(num_sms()), dim3(CF::kThreads), CF::smem_bytes(static_cast<int>(seg ? E : 1)), st, tA, tAS,
+                    tAC, tB, tBS, p);
 }
 
 // decode: few rows per expert, weight streaming; converted weights in tensor memory
@@ -864,6 +863,8 @@ using CfgPrefill = Cfg<128, 1, 8, 6, 8, 4, 2, true, 1, 2, 8, 1>;
 // C[m][n] = bf16(sum over s of partial[s][m][n]), four columns per thread.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ partial,
                                                             uint16_t* __restrict__ C, int64_t MN, int S) {
+  pdl_trigger();
+  pdl_wait();
   for (int64_t i = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) * 4; i < MN;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x * 4) {
     float4 acc = *reinterpret_cast<const float4*>(partial + i);
@@ -920,8 +921,8 @@ int gemm_common(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_
   if (rc != W4A8_OK || S == 1) return rc;
   const int64_t MN = M * N;  // N % 128 == 0, so MN % 4 == 0
   const int64_t blocks = ceil_div(MN / 4, 256) < 8 * 152 ? ceil_div(MN / 4, 256) : 8 * 152;
-  splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(partial, C, MN, S);
-  return check_launch("splitk_reduce_kernel");
+  return launch_pdl("splitk_reduce_kernel", splitk_reduce_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                    st, static_cast<const float*>(partial), C, MN, S);
 }
 
 }  // namespace

@@ -97,6 +97,8 @@ __device__ void place_pairs(const int32_t* __restrict__ ids, int f0, int f1, int
 __global__ void __launch_bounds__(kThreads, 1)
     permute_kernel(const int32_t* __restrict__ ids, int P, int E, int64_t* __restrict__ seg,
                    int32_t* __restrict__ src2dst, int32_t* __restrict__ dst2src) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ int sm[];
   int* run = sm;           // [E] counts, then running start of each expert
   int* wh = sm + E;        // [32][E] per-warp counts of the current chunk
@@ -132,6 +134,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Several CTAs, pass 1: CTA b counts the experts of pairs [b*C, (b+1)*C) into cnt[b][E].
 __global__ void __launch_bounds__(kThreads)
     permute_count_kernel(const int32_t* __restrict__ ids, int P, int E, int C, int* __restrict__ cnt) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ int hist[];
   const int tid = threadIdx.x;
   for (int i = tid; i < E; i += kThreads) hist[i] = 0;
@@ -156,6 +160,8 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kThreads, 1)
     permute_place_kernel(const int32_t* __restrict__ ids, int P, int E, int C, const int* __restrict__ cnt,
                          int64_t* __restrict__ seg, int32_t* __restrict__ src2dst, int32_t* __restrict__ dst2src) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ int sm[];
   int* run = sm;
   int* wh = sm + E;
@@ -231,17 +237,17 @@ extern "C" int moe_permute(const int32_t* topk_ids, int64_t T, int k, int64_t E,
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (need == 0) {
-    permute_kernel<<<1, kThreads, smem, st>>>(topk_ids, static_cast<int>(P), static_cast<int>(E), seg_indptr, src2dst,
-                                               dst2src);
-    return check_launch("permute_kernel");
+    return launch_pdl("permute_kernel", permute_kernel, dim3(1), dim3(kThreads), smem, st, topk_ids,
+                      static_cast<int>(P), static_cast<int>(E), seg_indptr, src2dst, dst2src);
   }
   const int C = static_cast<int>(permute_chunk(P));
   const int blocks = static_cast<int>((P + C - 1) / C);
   int* cnt = static_cast<int*>(ws);
-  permute_count_kernel<<<blocks, kThreads, static_cast<size_t>(E) * sizeof(int), st>>>(
-      topk_ids, static_cast<int>(P), static_cast<int>(E), C, cnt);
-  if (int rc = check_launch("permute_count_kernel")) return rc;
-  permute_place_kernel<<<blocks, kThreads, smem, st>>>(topk_ids, static_cast<int>(P), static_cast<int>(E), C, cnt,
-                                                       seg_indptr, src2dst, dst2src);
-  return check_launch("permute_place_kernel");
+  if (int rc = launch_pdl("permute_count_kernel", permute_count_kernel, dim3(blocks), dim3(kThreads),
+                          static_cast<size_t>(E) * sizeof(int), st, topk_ids, static_cast<int>(P),
+                          static_cast<int>(E), C, cnt))
+    return rc;
+  return launch_pdl("permute_place_kernel", permute_place_kernel, dim3(blocks), dim3(kThreads), smem, st, topk_ids,
+                    static_cast<int>(P), static_cast<int>(E), C, static_cast<const int*>(cnt), seg_indptr, src2dst,
+                    dst2src);
 }

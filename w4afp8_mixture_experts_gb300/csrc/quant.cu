@@ -50,6 +50,8 @@ __global__ void __launch_bounds__(256)
                       int64_t row_div, int64_t M_out, uint8_t* __restrict__ q, float* __restrict__ scales,
                       float* __restrict__ gcorr, int64_t ld) {
   constexpr int kQuantVals = kGroup / LANES;  // values per lane
+  pdl_trigger();
+  pdl_wait();
   const int64_t G = K / kGroup;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t task = tid / LANES;
@@ -123,6 +125,8 @@ __global__ void __launch_bounds__(256)
     silu_quad_kernel(const uint16_t* __restrict__ gu, int64_t M, int64_t I, uint8_t* __restrict__ q,
                      float* __restrict__ scales, float* __restrict__ gcorr, int64_t ld) {
   constexpr int kQuantVals = kGroup / LANES;  // values per lane
+  pdl_trigger();
+  pdl_wait();
   const int64_t G = I / kGroup;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t task = tid / LANES;
@@ -203,13 +207,9 @@ extern "C" int fp8_quant_per_token_group(const uint16_t* x, int64_t M_src, int64
   const bool small = groups < kSmallLaunchGroups;
   const int64_t blocks = ceil_div(groups * (small ? 16 : 4), 256);
   W4A8_REQUIRE(blocks < (1ll << 31), "too many rows");
-  if (small)
-    quant_quad_kernel<16><<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        x, K, row_index, row_div, M_out, q, scales, gcorr, scale_ld);
-  else
-    quant_quad_kernel<4><<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        x, K, row_index, row_div, M_out, q, scales, gcorr, scale_ld);
-  return check_launch("quant_quad_kernel");
+  return launch_pdl("quant_quad_kernel", small ? quant_quad_kernel<16> : quant_quad_kernel<4>,
+                    dim3(static_cast<unsigned>(blocks)), dim3(256), 0, static_cast<cudaStream_t>(stream), x, K,
+                    row_index, row_div, M_out, q, scales, gcorr, scale_ld);
 }
 
 extern "C" int silu_mul_requant(const uint16_t* gate_up, int64_t M, int64_t I, uint8_t* q, float* scales,
@@ -227,11 +227,7 @@ extern "C" int silu_mul_requant(const uint16_t* gate_up, int64_t M, int64_t I, u
   const bool small = groups < kSmallLaunchGroups;
   const int64_t blocks = ceil_div(groups * (small ? 16 : 4), 256);
   W4A8_REQUIRE(blocks < (1ll << 31), "too many rows");
-  if (small)
-    silu_quad_kernel<16><<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        gate_up, M, I, q, scales, gcorr, scale_ld);
-  else
-    silu_quad_kernel<4><<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        gate_up, M, I, q, scales, gcorr, scale_ld);
-  return check_launch("silu_quad_kernel");
+  return launch_pdl("silu_quad_kernel", small ? silu_quad_kernel<16> : silu_quad_kernel<4>,
+                    dim3(static_cast<unsigned>(blocks)), dim3(256), 0, static_cast<cudaStream_t>(stream), gate_up, M,
+                    I, q, scales, gcorr, scale_ld);
 }

@@ -11,6 +11,8 @@ template <int EPL>  // experts per lane
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                          int renorm, int32_t* __restrict__ ids,
                                                          float* __restrict__ w) {
+  pdl_trigger();
+  pdl_wait();
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -78,9 +80,8 @@ template <int EPL>
 int launch_route(const float* logits, int64_t T, int64_t E, int k, int renorm, int32_t* ids, float* w,
                  cudaStream_t st) {
   const int blocks = static_cast<int>(ceil_div(T, 8));
-  route_topk_kernel<EPL><<<blocks, 256, 0, st>>>(logits, static_cast<int>(T), static_cast<int>(E), k, renorm,
-                                                 ids, w);
-  return check_launch("route_topk_kernel");
+  return launch_pdl("route_topk_kernel", route_topk_kernel<EPL>, dim3(blocks), dim3(256), 0, st, logits,
+                    static_cast<int>(T), static_cast<int>(E), k, renorm, ids, w);
 }
 
 }  // namespace
