@@ -124,6 +124,22 @@ struct Cfg {
   static_assert(EPIS_ == 1 || EPIS_ == 2, "one or two epilogue sets");
   static_assert(EPIW_ % (4 * EPIS_) == 0, "each epilogue set covers all four lane quarters");
   static_assert(kOffSched + 2 * 257 * 4 + 1024 <= 227 * 1024, "shared memory (256 experts)");
+  // Wide tiles promote from 16x256b fragments: each epilogue thread holds 4 rows x 16 columns of a
+  // 64-column block, so a token scale read from shared memory serves 4 rows (a 32x32b fragment, one
+  // row per thread, makes every column's scale a 32-lane broadcast).  The fragments and the 64
+  // accumulators need more registers than an even split gives, so these tiles also move registers
+  // from the producer/MMA warpgroup and the converters to the epilogue warpgroups.
+  static constexpr int kEpiCols = NMAX_ * 4 / (EPIW_ / EPIS_);  // columns per epilogue warp
+  static constexpr bool kEpi16 = NMAX_ >= 64 && EPIS_ == 1 && kEpiCols % 64 == 0;
+  static constexpr bool kRegSplit = kEpi16;
+  static constexpr int kRegsCtl = 64;    // warps 0-3: the two producers and the MMA warps
+  static constexpr int kRegsConv = 96;   // converter warpgroups
+  static constexpr int kRegsEpi = 176;   // epilogue warpgroups
+  static_assert(!kRegSplit || (kThreads == 512 && kWarpConv0 == 4 && kWarpEpi0 % 4 == 0),
+                "register split: warp roles aligned to warpgroups, 512 threads");
+  static_assert(!kRegSplit || 128 * kRegsCtl + 32 * kConvSets * kConvWarps * kRegsConv + 32 * EPIW_ * kRegsEpi <=
+                                  kThreads * 128,
+                "register split exceeds the registers the block is launched with");
 };
 
 struct GemmParams {
@@ -253,6 +269,15 @@ __device__ __forceinline__ void promote2(uint64_t& acc2, uint64_t ws2, float t0,
   asm("mov.b64 %0, {%1, %2};" : "=l"(ks) : "f"(k0), "f"(k1));
   asm("mov.b64 %0, {%1, %2};" : "=l"(pp) : "r"(p0), "r"(p1));
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(ts), "l"(pp), "l"(ks));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2) : "l"(ws2), "l"(e));
+}
+
+// The same promotion with the token scales and corrections already packed in pairs.
+__device__ __forceinline__ void promote2p(uint64_t& acc2, uint64_t ws2, uint64_t ts2, uint64_t ks2, uint32_t p0,
+                                          uint32_t p1) {
+  uint64_t e, pp;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pp) : "r"(p0), "r"(p1));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(ts2), "l"(pp), "l"(ks2));
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2) : "l"(ws2), "l"(e));
 }
 
@@ -388,106 +413,112 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
   // Counters: `it` counts 128-K groups, `st` counts stages of gps groups; stage st holds
   // groups [st*gps, st*gps + gps) of one tile (gps divides K/128, so stages never straddle
   // tiles).  A tile covers token rows [row0 & ~3, ...): the scale vectors start 16-byte aligned.
-  if (warp == kWarpTma) {
-    // ---- weight ring producer: runs ahead of everything else ----
-    if (lane == 0) {
-      const uint64_t pol_w = l2_policy_evict_first();
-      const uint32_t w_bytes = gps * CF::kWpkBytes;
-      uint32_t st = 0;
-      for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        int e, nb, row0, rows;
-        sch.decode(item, e, nb, row0, rows);
-        int g_beg, g_end;
-        sch.krange(item, g_beg, g_end);
-        for (int g0 = g_beg; g0 < g_end; g0 += gps, ++st) {
-          const int s = st % STAGES;
-          const uint32_t ph = (st / STAGES) & 1;
-          if (!wait_bar(&empty[s], ph ^ 1, s_abort)) goto done;
-          mbar_arrive_expect_tx(&full[s], w_bytes);
-          tma_load_3d_hint(s_wpk + s * GPS * CF::kWpkBytes, &tmB, &full[s], 0, e * prm.N + nb * kBM, g0, pol_w);
+  // Warp roles, grouped by warpgroup; with a register split every warp of a warpgroup first executes
+  // the same setmaxnreg instruction.
+  if (warp < kWarpConv0) {
+    if constexpr (CF::kRegSplit) regs_release<CF::kRegsCtl>();
+    if (warp == kWarpTma) {
+      // ---- weight ring producer: runs ahead of everything else ----
+      if (lane == 0) {
+        const uint64_t pol_w = l2_policy_evict_first();
+        const uint32_t w_bytes = gps * CF::kWpkBytes;
+        uint32_t st = 0;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+          int e, nb, row0, rows;
+          sch.decode(item, e, nb, row0, rows);
+          int g_beg, g_end;
+          sch.krange(item, g_beg, g_end);
+          for (int g0 = g_beg; g0 < g_end; g0 += gps, ++st) {
+            const int s = st % STAGES;
+            const uint32_t ph = (st / STAGES) & 1;
+            if (!wait_bar(&empty[s], ph ^ 1, s_abort)) goto done;
+            mbar_arrive_expect_tx(&full[s], w_bytes);
+            tma_load_3d_hint(s_wpk + s * GPS * CF::kWpkBytes, &tmB, &full[s], 0, e * prm.N + nb * kBM, g0, pol_w);
+          }
         }
       }
-    }
-  } else if (warp == kWarpTmaAct) {
-    // ---- token and scale ring producer ----
-    if (lane == 0) {
-      const uint32_t t_bytes = gps * CF::kTokBytes;
-      const uint32_t sc_bytes = gps * (2 * NMAX * 4 + kBM * 4);
-      uint32_t st = 0;
-      for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        int e, nb, row0, rows;
-        sch.decode(item, e, nb, row0, rows);
-        const int r4 = row0 & ~3;
-        int g_beg, g_end;
-        sch.krange(item, g_beg, g_end);
-        for (int g0 = g_beg; g0 < g_end; g0 += gps, ++st) {
-          const int ts_ = st % TSTAGES;
-          const uint32_t tph = (st / TSTAGES) & 1;
-          const int ss = st % SSTAGES;
-          const uint32_t sph = (st / SSTAGES) & 1;
-          if (!wait_bar(&tempty[ts_], tph ^ 1, s_abort)) goto done;
-          mbar_arrive_expect_tx(&tfull[ts_], t_bytes);
-          tma_load_3d(s_tok + ts_ * GPS * CF::kTokBytes, &tmA, &tfull[ts_], 0, r4, g0);
-          if (!wait_bar(&sempty[ss], sph ^ 1, s_abort)) goto done;
-          uint8_t* sc = s_sc + ss * CF::kScBytes;
-          mbar_arrive_expect_tx(&sfull[ss], sc_bytes);
-          tma_load_2d(sc, &tmAS, &sfull[ss], r4, g0);
-          tma_load_2d(sc + CF::kTscBytes, &tmAC, &sfull[ss], r4, g0);
-          tma_load_2d(sc + 2 * CF::kTscBytes, &tmBS, &sfull[ss], nb * kBM, e * G + g0);
+    } else if (warp == kWarpTmaAct) {
+      // ---- token and scale ring producer ----
+      if (lane == 0) {
+        const uint32_t t_bytes = gps * CF::kTokBytes;
+        const uint32_t sc_bytes = gps * (2 * NMAX * 4 + kBM * 4);
+        uint32_t st = 0;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+          int e, nb, row0, rows;
+          sch.decode(item, e, nb, row0, rows);
+          const int r4 = row0 & ~3;
+          int g_beg, g_end;
+          sch.krange(item, g_beg, g_end);
+          for (int g0 = g_beg; g0 < g_end; g0 += gps, ++st) {
+            const int ts_ = st % TSTAGES;
+            const uint32_t tph = (st / TSTAGES) & 1;
+            const int ss = st % SSTAGES;
+            const uint32_t sph = (st / SSTAGES) & 1;
+            if (!wait_bar(&tempty[ts_], tph ^ 1, s_abort)) goto done;
+            mbar_arrive_expect_tx(&tfull[ts_], t_bytes);
+            tma_load_3d(s_tok + ts_ * GPS * CF::kTokBytes, &tmA, &tfull[ts_], 0, r4, g0);
+            if (!wait_bar(&sempty[ss], sph ^ 1, s_abort)) goto done;
+            uint8_t* sc = s_sc + ss * CF::kScBytes;
+            mbar_arrive_expect_tx(&sfull[ss], sc_bytes);
+            tma_load_2d(sc, &tmAS, &sfull[ss], r4, g0);
+            tma_load_2d(sc + CF::kTscBytes, &tmAC, &sfull[ss], r4, g0);
+            tma_load_2d(sc + 2 * CF::kTscBytes, &tmBS, &sfull[ss], nb * kBM, e * G + g0);
+          }
         }
       }
-    }
-  } else if (warp < kWarpConv0) {
-    // ---- MMA issue: every stage; warp m issues the groups j with j % kMmaWarps == m ----
-    const int mset = warp - kWarpMma;
-    if (lane == 0) {
-      uint32_t st = 0;
-      for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        int e, nb, row0, rows;
-        sch.decode(item, e, nb, row0, rows);
-        const int ncol = (row0 - (row0 & ~3) + rows + 15) & ~15;
-        const uint32_t idesc = idesc_e4m3(static_cast<uint32_t>(ncol));
-        int g_beg, g_end;
-        sch.krange(item, g_beg, g_end);
-        for (int g0 = g_beg; g0 < g_end; g0 += gps, ++st) {
-          const int ts_ = st % TSTAGES;
-          const uint32_t tph = (st / TSTAGES) & 1;
-          const int a = st % ABUF;
-          const uint32_t aph = (st / ABUF) & 1;
-          const int pslot = st % NP;
-          const uint32_t pph = (st / NP) & 1;
-          // token tiles landed, weights converted, partial slot read by the epilogue
-          const bool ok = mbar_test3(&tfull[ts_], tph, &mready[a], aph, &pempty[pslot], pph ^ 1) ||
-                          (wait_bar(&tfull[ts_], tph, s_abort) && wait_bar(&mready[a], aph, s_abort) &&
-                           wait_bar(&pempty[pslot], pph ^ 1, s_abort));
-          if (!ok) goto done;
-          tc_fence_after();
+    } else {
+      // ---- MMA issue: every stage; warp m issues the groups j with j % kMmaWarps == m ----
+      const int mset = warp - kWarpMma;
+      if (lane == 0) {
+        uint32_t st = 0;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+          int e, nb, row0, rows;
+          sch.decode(item, e, nb, row0, rows);
+          const int ncol = (row0 - (row0 & ~3) + rows + 15) & ~15;
+          const uint32_t idesc = idesc_e4m3(static_cast<uint32_t>(ncol));
+          int g_beg, g_end;
+          sch.krange(item, g_beg, g_end);
+          for (int g0 = g_beg; g0 < g_end; g0 += gps, ++st) {
+            const int ts_ = st % TSTAGES;
+            const uint32_t tph = (st / TSTAGES) & 1;
+            const int a = st % ABUF;
+            const uint32_t aph = (st / ABUF) & 1;
+            const int pslot = st % NP;
+            const uint32_t pph = (st / NP) & 1;
+            // token tiles landed, weights converted, partial slot read by the epilogue
+            const bool ok = mbar_test3(&tfull[ts_], tph, &mready[a], aph, &pempty[pslot], pph ^ 1) ||
+                            (wait_bar(&tfull[ts_], tph, s_abort) && wait_bar(&mready[a], aph, s_abort) &&
+                             wait_bar(&pempty[pslot], pph ^ 1, s_abort));
+            if (!ok) goto done;
+            tc_fence_after();
 #pragma unroll
-          for (int j = 0; j < GPS; ++j) {
-            if (j >= gps) break;
-            if (j % CF::kMmaWarps != mset) continue;
-            const uint32_t d = tmem_base + (pslot * GPS + j) * NMAX;
-            const uint32_t tok = smem_u32(s_tok + (ts_ * GPS + j) * CF::kTokBytes);
+            for (int j = 0; j < GPS; ++j) {
+              if (j >= gps) break;
+              if (j % CF::kMmaWarps != mset) continue;
+              const uint32_t d = tmem_base + (pslot * GPS + j) * NMAX;
+              const uint32_t tok = smem_u32(s_tok + (ts_ * GPS + j) * CF::kTokBytes);
 #pragma unroll
-            for (int kk = 0; kk < kGroup / kKStep; ++kk) {
-              const uint64_t bdesc = sw128_desc(tok + kk * kKStep);
-              if constexpr (CF::A_TMEM) {
-                const uint32_t a_t = tmem_base + CF::kAColBase + (a * GPS + j) * 32 + kk * (kKStep / 4);
-                mma_f8f6f4_ts(d, a_t, bdesc, idesc, kk > 0 ? 1u : 0u);
-              } else {
-                const uint64_t adesc = sw128_desc(smem_u32(s_a + (a * GPS + j) * CF::kABytes) + kk * kKStep);
-                mma_f8f6f4_ss(d, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < kGroup / kKStep; ++kk) {
+                const uint64_t bdesc = sw128_desc(tok + kk * kKStep);
+                if constexpr (CF::A_TMEM) {
+                  const uint32_t a_t = tmem_base + CF::kAColBase + (a * GPS + j) * 32 + kk * (kKStep / 4);
+                  mma_f8f6f4_ts(d, a_t, bdesc, idesc, kk > 0 ? 1u : 0u);
+                } else {
+                  const uint64_t adesc = sw128_desc(smem_u32(s_a + (a * GPS + j) * CF::kABytes) + kk * kKStep);
+                  mma_f8f6f4_ss(d, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+                }
               }
             }
+            // a commit arrives once this thread's earlier MMAs are complete (at once if it issued none)
+            mma_commit(&pfull[pslot]);
+            mma_commit(&mdone[a]);
+            mma_commit(&tempty[ts_]);
           }
-          // a commit arrives once this thread's earlier MMAs are complete (at once if it issued none)
-          mma_commit(&pfull[pslot]);
-          mma_commit(&mdone[a]);
-          mma_commit(&tempty[ts_]);
         }
       }
     }
   } else if (warp < kWarpEpi0) {
+    if constexpr (CF::kRegSplit) regs_release<CF::kRegsConv>();
     // ---- converters: every stage; set c converts the groups j with j % kConvSets == c ----
     const int q4 = warp & 3;
     const int cset = (warp - kWarpConv0) / kConvWarps;
@@ -563,134 +594,240 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
       }
     }
   } else {
-    // ---- promotion and epilogue ----
-    // Warp w: lane quarter q4 = w & 3, epilogue set `eset` (the groups j of every stage with
-    // j % EPIS == eset) and, within the set, column block `half`.
-    const int ew = warp - kWarpEpi0;
-    const int q4 = warp & 3;
-    const int eset = ew / CF::kEpiSetWarps;
-    const int half = (ew % CF::kEpiSetWarps) >> 2;
-    const int r = q4 * 32 + lane;
-    const int c0 = half * NHALF;
-    const uint32_t t_lane = static_cast<uint32_t>(q4 * 32) << 16;
-    constexpr int CH = NHALF < 16 ? 8 : 16;  // columns per tensor-memory load
-    uint32_t st = 0, tile = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++tile) {
-      int e, nb, row0, rows;
-      sch.decode(item, e, nb, row0, rows);
-      const int r4 = row0 & ~3;
-      const int lo = row0 - r4;   // columns [lo, lo + rows) of the tile are this chunk's rows
-      const int need = lo + rows;  // columns past `need` are never stored: skip their promotion
-      uint64_t acc2[NHALF / 2];   // packed pairs of fp32 accumulators
+    if constexpr (CF::kRegSplit) regs_claim<CF::kRegsEpi>();
+    if constexpr (CF::kEpi16) {
+      // 16x256b fragments: thread t of the warp for lane quarter q4 and column block `half` holds,
+      // for each 64-column block b, rows q4*32 + t/4 + 8*rho (rho = 0..3) and columns
+      // c0 + 64*b + 8*v + 2*(t%4) + {0, 1} (v = 0..7): a token scale pair read from shared memory
+      // serves four rows.  Same promotion, same order of groups as the 32x32b path below.
+      constexpr int NB = NHALF / 64;
+      const int ew = warp - kWarpEpi0;
+      const int q4 = warp & 3;
+      const int c0 = (ew >> 2) * NHALF;
+      const int rq = q4 * 32 + (lane >> 2);
+      const int cq = 2 * (lane & 3);
+      const uint32_t t_lane = static_cast<uint32_t>(q4 * 32) << 16;
+      uint32_t st = 0;
+      for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        int e, nb, row0, rows;
+        sch.decode(item, e, nb, row0, rows);
+        const int r4 = row0 & ~3;
+        const int lo = row0 - r4;    // columns [lo, lo + rows) of the tile are this chunk's rows
+        const int need = lo + rows;  // 64-column blocks from `need` on are never stored: skipped
+        uint64_t acc2[NB][4][8];
 #pragma unroll
-      for (int q = 0; q < NHALF / 2; ++q) acc2[q] = 0ull;
-      int g_beg, g_end;
-      sch.krange(item, g_beg, g_end);
-      for (int g0 = g_beg; g0 < g_end; g0 += gps, ++st) {
-        const int ss = st % SSTAGES;
-        const uint32_t sph = (st / SSTAGES) & 1;
-        const int pslot = st % NP;
-        const uint32_t pph = (st / NP) & 1;
-        const float* tsc = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes);
-        const float* tcr = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes + CF::kTscBytes);
-        const float* wsc = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes + 2 * CF::kTscBytes);
-        bool ok = true;
-        if (!mbar_try_wait(&sfull[ss], sph) || !mbar_try_wait(&pfull[pslot], pph))
-          ok = wait_bar(&sfull[ss], sph, s_abort) && wait_bar(&pfull[pslot], pph, s_abort);
-        if (__any_sync(0xffffffffu, !ok)) goto done;  // warp converged below
-        tc_fence_after();
+        for (int b = 0; b < NB; ++b)
 #pragma unroll
-        for (int j = 0; j < GPS; ++j) {
-          if (j >= gps) break;
-          if (EPIS > 1 && j % EPIS != eset) continue;
-          const float ws = wsc[j * kBM + r];
-          uint64_t ws2;
-          asm("mov.b64 %0, {%1, %1};" : "=l"(ws2) : "f"(ws));
-          const float* ts = tsc + j * NMAX;
-          const float* tc = tcr + j * NMAX;
+          for (int rho = 0; rho < 4; ++rho)
 #pragma unroll
-          for (int c = 0; c < NHALF; c += CH) {
-            if (c0 + c >= need) continue;  // warp-uniform
-            uint32_t p[CH];
-            tmem_load_cols<CH>(tmem_base + t_lane + (pslot * GPS + j) * NMAX + c0 + c, p);
-            tmem_wait_ld();
+            for (int v = 0; v < 8; ++v) acc2[b][rho][v] = 0ull;
+        int g_beg, g_end;
+        sch.krange(item, g_beg, g_end);
+        for (int g0 = g_beg; g0 < g_end; g0 += gps, ++st) {
+          const int ss = st % SSTAGES;
+          const uint32_t sph = (st / SSTAGES) & 1;
+          const int pslot = st % NP;
+          const uint32_t pph = (st / NP) & 1;
+          const float* tsc = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes);
+          const float* tcr = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes + CF::kTscBytes);
+          const float* wsc = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes + 2 * CF::kTscBytes);
+          bool ok = true;
+          if (!mbar_try_wait(&sfull[ss], sph) || !mbar_try_wait(&pfull[pslot], pph))
+            ok = wait_bar(&sfull[ss], sph, s_abort) && wait_bar(&pfull[pslot], pph, s_abort);
+          if (__any_sync(0xffffffffu, !ok)) goto done;  // warp converged below
+          tc_fence_after();
 #pragma unroll
-            for (int q = 0; q < CH; q += 4) {
-              const float4 t = *reinterpret_cast<const float4*>(ts + c0 + c + q);
-              const float4 k = *reinterpret_cast<const float4*>(tc + c0 + c + q);
-              promote2(acc2[(c + q) / 2], ws2, t.x, t.y, k.x, k.y, p[q], p[q + 1]);
-              promote2(acc2[(c + q) / 2 + 1], ws2, t.z, t.w, k.z, k.w, p[q + 2], p[q + 3]);
+          for (int j = 0; j < GPS; ++j) {
+            if (j >= gps) break;
+            const float* wsj = wsc + j * kBM + rq;
+            const float* ts = tsc + j * NMAX + c0 + cq;
+            const float* tc = tcr + j * NMAX + c0 + cq;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+              if (c0 + 64 * b >= need) continue;  // warp-uniform
+              uint32_t p[64];
+              const uint32_t pa = tmem_base + t_lane + (pslot * GPS + j) * NMAX + c0 + 64 * b;
+              tmem_ld16x256b_x8(pa, p);                    // lanes q4*32 + 0 .. 15
+              tmem_ld16x256b_x8(pa + (16u << 16), p + 32);  // lanes q4*32 + 16 .. 31
+              uint64_t ws2[4];
+#pragma unroll
+              for (int rho = 0; rho < 4; ++rho) {
+                const float w = wsj[8 * rho];
+                asm("mov.b64 %0, {%1, %1};" : "=l"(ws2[rho]) : "f"(w));
+              }
+              tmem_wait_ld_pin<64>(p);
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                const uint64_t t2 = *reinterpret_cast<const uint64_t*>(ts + 64 * b + 8 * v);
+                const uint64_t k2 = *reinterpret_cast<const uint64_t*>(tc + 64 * b + 8 * v);
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                  for (int jj = 0; jj < 2; ++jj) {
+                    const int i = 32 * h + 4 * v + 2 * jj;
+                    promote2p(acc2[b][2 * h + jj][v], ws2[2 * h + jj], t2, k2, p[i], p[i + 1]);
+                  }
+              }
             }
           }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&pempty[pslot]);
+            mbar_arrive(&sempty[ss]);
+          }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&pempty[pslot]);
-          mbar_arrive(&sempty[ss]);
-        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+#pragma unroll
+          for (int rho = 0; rho < 4; ++rho)
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              float a[2];
+              asm("mov.b64 {%0, %1}, %2;" : "=f"(a[0]), "=f"(a[1]) : "l"(acc2[b][rho][v]));
+              const int n = nb * kBM + rq + 8 * rho;  // output column: weight row of the block
+#pragma unroll
+              for (int q = 0; q < 2; ++q) {
+                const int t = c0 + 64 * b + 8 * v + cq + q;  // tile column: token row r4 + t
+                if (t < lo || t >= need) continue;
+                const int64_t m = r4 + t;
+                if (SPLIT)
+                  prm.partial[(static_cast<int64_t>(item % sch.S) * prm.M + m) * prm.N + n] = a[q];
+                else
+                  prm.C[m * prm.N + n] = float_to_bf16_bits(a[q]);
+              }
+            }
       }
-      if constexpr (EPIS > 1) {
-        // Set 1 hands its partial sums to set 0 through tensor memory (same lane quarter and
-        // columns); slot = tile parity, guarded by xfull / xempty.
-        const int xs = tile & 1;
-        const uint32_t xph = (tile >> 1) & 1;
-        const uint32_t xaddr = tmem_base + t_lane + CF::kXColBase + xs * NMAX + c0;
-        if (eset != 0) {
-          if (__any_sync(0xffffffffu, !wait_bar(&xempty[xs], xph ^ 1, s_abort))) goto done;
+    } else {
+      // ---- promotion and epilogue ----
+      // Warp w: lane quarter q4 = w & 3, epilogue set `eset` (the groups j of every stage with
+      // j % EPIS == eset) and, within the set, column block `half`.
+      const int ew = warp - kWarpEpi0;
+      const int q4 = warp & 3;
+      const int eset = ew / CF::kEpiSetWarps;
+      const int half = (ew % CF::kEpiSetWarps) >> 2;
+      const int r = q4 * 32 + lane;
+      const int c0 = half * NHALF;
+      const uint32_t t_lane = static_cast<uint32_t>(q4 * 32) << 16;
+      constexpr int CH = NHALF < 16 ? 8 : 16;  // columns per tensor-memory load
+      uint32_t st = 0, tile = 0;
+      for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++tile) {
+        int e, nb, row0, rows;
+        sch.decode(item, e, nb, row0, rows);
+        const int r4 = row0 & ~3;
+        const int lo = row0 - r4;   // columns [lo, lo + rows) of the tile are this chunk's rows
+        const int need = lo + rows;  // columns past `need` are never stored: skip their promotion
+        uint64_t acc2[NHALF / 2];   // packed pairs of fp32 accumulators
+#pragma unroll
+        for (int q = 0; q < NHALF / 2; ++q) acc2[q] = 0ull;
+        int g_beg, g_end;
+        sch.krange(item, g_beg, g_end);
+        for (int g0 = g_beg; g0 < g_end; g0 += gps, ++st) {
+          const int ss = st % SSTAGES;
+          const uint32_t sph = (st / SSTAGES) & 1;
+          const int pslot = st % NP;
+          const uint32_t pph = (st / NP) & 1;
+          const float* tsc = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes);
+          const float* tcr = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes + CF::kTscBytes);
+          const float* wsc = reinterpret_cast<const float*>(s_sc + ss * CF::kScBytes + 2 * CF::kTscBytes);
+          bool ok = true;
+          if (!mbar_try_wait(&sfull[ss], sph) || !mbar_try_wait(&pfull[pslot], pph))
+            ok = wait_bar(&sfull[ss], sph, s_abort) && wait_bar(&pfull[pslot], pph, s_abort);
+          if (__any_sync(0xffffffffu, !ok)) goto done;  // warp converged below
+          tc_fence_after();
+#pragma unroll
+          for (int j = 0; j < GPS; ++j) {
+            if (j >= gps) break;
+            if (EPIS > 1 && j % EPIS != eset) continue;
+            const float ws = wsc[j * kBM + r];
+            uint64_t ws2;
+            asm("mov.b64 %0, {%1, %1};" : "=l"(ws2) : "f"(ws));
+            const float* ts = tsc + j * NMAX;
+            const float* tc = tcr + j * NMAX;
+#pragma unroll
+            for (int c = 0; c < NHALF; c += CH) {
+              if (c0 + c >= need) continue;  // warp-uniform
+              uint32_t p[CH];
+              tmem_load_cols<CH>(tmem_base + t_lane + (pslot * GPS + j) * NMAX + c0 + c, p);
+              tmem_wait_ld();
+#pragma unroll
+              for (int q = 0; q < CH; q += 4) {
+                const float4 t = *reinterpret_cast<const float4*>(ts + c0 + c + q);
+                const float4 k = *reinterpret_cast<const float4*>(tc + c0 + c + q);
+                promote2(acc2[(c + q) / 2], ws2, t.x, t.y, k.x, k.y, p[q], p[q + 1]);
+                promote2(acc2[(c + q) / 2 + 1], ws2, t.z, t.w, k.z, k.w, p[q + 2], p[q + 3]);
+              }
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&pempty[pslot]);
+            mbar_arrive(&sempty[ss]);
+          }
+        }
+        if constexpr (EPIS > 1) {
+          // Set 1 hands its partial sums to set 0 through tensor memory (same lane quarter and
+          // columns); slot = tile parity, guarded by xfull / xempty.
+          const int xs = tile & 1;
+          const uint32_t xph = (tile >> 1) & 1;
+          const uint32_t xaddr = tmem_base + t_lane + CF::kXColBase + xs * NMAX + c0;
+          if (eset != 0) {
+            if (__any_sync(0xffffffffu, !wait_bar(&xempty[xs], xph ^ 1, s_abort))) goto done;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < NHALF; c += 8) {
+              uint32_t v[8];
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                asm("mov.b64 {%0, %1}, %2;" : "=r"(v[2 * q]), "=r"(v[2 * q + 1]) : "l"(acc2[c / 2 + q]));
+              tmem_st8(xaddr + c, v);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xfull[xs]);
+            continue;
+          }
+          if (__any_sync(0xffffffffu, !wait_bar(&xfull[xs], xph, s_abort))) goto done;
           tc_fence_after();
 #pragma unroll
           for (int c = 0; c < NHALF; c += 8) {
             uint32_t v[8];
+            tmem_ld8(xaddr + c, v);
+            tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              asm("mov.b64 {%0, %1}, %2;" : "=r"(v[2 * q]), "=r"(v[2 * q + 1]) : "l"(acc2[c / 2 + q]));
-            tmem_st8(xaddr + c, v);
+            for (int q = 0; q < 4; ++q) {
+              uint64_t o;
+              asm("mov.b64 %0, {%1, %2};" : "=l"(o) : "r"(v[2 * q]), "r"(v[2 * q + 1]));
+              asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc2[c / 2 + q]) : "l"(o));
+            }
           }
-          tmem_wait_st();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&xfull[xs]);
+          if (lane == 0) mbar_arrive(&xempty[xs]);
+        }
+        if (SPLIT) {  // split-K: fp32 partial sums of this split, reduced by a second kernel
+          float* prow = prm.partial + (static_cast<int64_t>(item % sch.S) * prm.M + r4) * prm.N + nb * kBM + r;
+#pragma unroll
+          for (int q = 0; q < NHALF / 2; ++q) {
+            float a0, a1;
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc2[q]));
+            const int t = c0 + 2 * q;
+            if (t >= lo && t < lo + rows) prow[static_cast<int64_t>(t) * prm.N] = a0;
+            if (t + 1 >= lo && t + 1 < lo + rows) prow[static_cast<int64_t>(t + 1) * prm.N] = a1;
+          }
           continue;
         }
-        if (__any_sync(0xffffffffu, !wait_bar(&xfull[xs], xph, s_abort))) goto done;
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < NHALF; c += 8) {
-          uint32_t v[8];
-          tmem_ld8(xaddr + c, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint64_t o;
-            asm("mov.b64 %0, {%1, %2};" : "=l"(o) : "r"(v[2 * q]), "r"(v[2 * q + 1]));
-            asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc2[c / 2 + q]) : "l"(o));
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&xempty[xs]);
-      }
-      if (SPLIT) {  // split-K: fp32 partial sums of this split, reduced by a second kernel
-        float* prow = prm.partial + (static_cast<int64_t>(item % sch.S) * prm.M + r4) * prm.N + nb * kBM + r;
+        uint16_t* crow = prm.C + static_cast<int64_t>(r4) * prm.N + nb * kBM + r;
 #pragma unroll
         for (int q = 0; q < NHALF / 2; ++q) {
           float a0, a1;
           asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc2[q]));
           const int t = c0 + 2 * q;
-          if (t >= lo && t < lo + rows) prow[static_cast<int64_t>(t) * prm.N] = a0;
-          if (t + 1 >= lo && t + 1 < lo + rows) prow[static_cast<int64_t>(t + 1) * prm.N] = a1;
+          if (t >= lo && t < lo + rows) crow[static_cast<int64_t>(t) * prm.N] = float_to_bf16_bits(a0);
+          if (t + 1 >= lo && t + 1 < lo + rows) crow[static_cast<int64_t>(t + 1) * prm.N] = float_to_bf16_bits(a1);
         }
-        continue;
-      }
-      uint16_t* crow = prm.C + static_cast<int64_t>(r4) * prm.N + nb * kBM + r;
-#pragma unroll
-      for (int q = 0; q < NHALF / 2; ++q) {
-        float a0, a1;
-        asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc2[q]));
-        const int t = c0 + 2 * q;
-        if (t >= lo && t < lo + rows) crow[static_cast<int64_t>(t) * prm.N] = float_to_bf16_bits(a0);
-        if (t + 1 >= lo && t + 1 < lo + rows) crow[static_cast<int64_t>(t + 1) * prm.N] = float_to_bf16_bits(a1);
       }
     }
   }
@@ -838,6 +975,21 @@ int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, c
         cudaFuncSetAttribute(w4a8_gemm_kernel<CF, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              CF::kSmemBytesMax) != cudaSuccess)
       return check_launch("cudaFuncSetAttribute(gemm)");
+    if constexpr (CF::kRegSplit) {
+      // setmaxnreg.inc waits until the released registers cover the request: the warpgroups'
+      // budgets must fit in what the block is launched with, or the claim would never return.
+      for (int sp = 0; sp < 2; ++sp) {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, sp ? w4a8_gemm_kernel<CF, true> : w4a8_gemm_kernel<CF, false>) !=
+            cudaSuccess)
+          return check_launch("cudaFuncGetAttributes(gemm)");
+        const int need = 128 * CF::kRegsCtl + 32 * CF::kConvSets * kConvWarps * CF::kRegsConv +
+                         32 * CF::kEpiWarps * CF::kRegsEpi;
+        if (fa.numRegs * CF::kThreads < need)
+          return set_error(W4A8_ERR_UNSUPPORTED, "gemm kernel built with %d registers per thread: %d < %d",
+                           fa.numRegs, fa.numRegs * CF::kThreads, need);
+      }
+    }
     attr_set = true;
   }
   GemmParams p;
