@@ -132,6 +132,16 @@ struct Cfg {
   static constexpr int kEpiCols = NMAX_ * 4 / (EPIW_ / EPIS_);  // columns per epilogue warp
   static constexpr bool kEpi16 = NMAX_ >= 64 && EPIS_ == 1 && kEpiCols % 64 == 0;
   static constexpr bool kRegSplit = kEpi16;
+  // With one group per stage the MMA warps take whole stages in turn (warp m: stages st % MMAS == m)
+  // instead of groups of a stage, and each stage's barriers get one commit.  A token or A slot is
+  // then committed by one MMA warp only (its ring depth is a multiple of MMAS), so its phases
+  // complete in order.  A partial slot may pass between MMA warps: the MMAs of stage st + NP wait
+  // until the epilogue has read stage st, so its phases complete in order too, and an MMA warp
+  // waiting on it is never two phases behind.
+  static constexpr bool kMmaByStage = GPS_ == 1 && MMAS_ > 1;
+  static constexpr int kMmaCommits = kMmaByStage ? 1 : MMAS_;
+  static_assert(!kMmaByStage || (TSTAGES_ % MMAS_ == 0 && ABUF_ % MMAS_ == 0),
+                "stage-wise MMA warps: token and A ring depths must be multiples of the MMA warps");
   static constexpr int kRegsCtl = 64;    // warps 0-3: the two producers and the MMA warps
   static constexpr int kRegsConv = 96;   // converter warpgroups
   static constexpr int kRegsEpi = 176;   // epilogue warpgroups
@@ -340,7 +350,7 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
     }
     for (int s = 0; s < TSTAGES; ++s) {
       mbar_init(&tfull[s], 1);
-      mbar_init(&tempty[s], CF::kMmaWarps);  // one commit per MMA warp
+      mbar_init(&tempty[s], CF::kMmaCommits);  // one commit per MMA warp taking part in the stage
     }
     for (int s = 0; s < SSTAGES; ++s) {
       mbar_init(&sfull[s], 1);
@@ -348,10 +358,10 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
     }
     for (int b = 0; b < ABUF; ++b) {
       mbar_init(&mready[b], kConvSets * kConvWarps);
-      mbar_init(&mdone[b], CF::kMmaWarps);
+      mbar_init(&mdone[b], CF::kMmaCommits);
     }
     for (int b = 0; b < NP; ++b) {
-      mbar_init(&pfull[b], CF::kMmaWarps);
+      mbar_init(&pfull[b], CF::kMmaCommits);
       mbar_init(&pempty[b], CF::kEpiWarps);
     }
     for (int b = 0; b < 2; ++b) {
@@ -467,7 +477,8 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
         }
       }
     } else {
-      // ---- MMA issue: every stage; warp m issues the groups j with j % kMmaWarps == m ----
+      // ---- MMA issue: every stage, warp m issuing the groups j with j % kMmaWarps == m; with one
+      // group per stage, the stages st with st % kMmaWarps == m ----
       const int mset = warp - kWarpMma;
       if (lane == 0) {
         uint32_t st = 0;
@@ -479,6 +490,9 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
           int g_beg, g_end;
           sch.krange(item, g_beg, g_end);
           for (int g0 = g_beg; g0 < g_end; g0 += gps, ++st) {
+            if constexpr (CF::kMmaByStage) {
+              if (static_cast<int>(st % CF::kMmaWarps) != mset) continue;
+            }
             const int ts_ = st % TSTAGES;
             const uint32_t tph = (st / TSTAGES) & 1;
             const int a = st % ABUF;
@@ -494,7 +508,7 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
 #pragma unroll
             for (int j = 0; j < GPS; ++j) {
               if (j >= gps) break;
-              if (j % CF::kMmaWarps != mset) continue;
+              if (!CF::kMmaByStage && j % CF::kMmaWarps != mset) continue;
               const uint32_t d = tmem_base + (pslot * GPS + j) * NMAX;
               const uint32_t tok = smem_u32(s_tok + (ts_ * GPS + j) * CF::kTokBytes);
 #pragma unroll
