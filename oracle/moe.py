@@ -132,7 +132,7 @@ def route_topk(logits, k: int, renormalize: bool = True):
 # ----------------------------------------------------------------------------
 # (2) permutation preprocess
 
-def permute(topk_ids, E: int):
+def permute(topk_ids, E: int, expert_map=None):
     """Stable sort of the flat routed pairs f = t*k + j by expert.
 
     SGLang PR #7762 page, review of ep_moe/kernels.py: the preprocess sorts
@@ -140,14 +140,32 @@ def permute(topk_ids, E: int):
     (int64 segment starts of each expert) and src2dst (position of each flat
     pair in sorted order).  Returns seg_indptr int64 [E+1], src2dst int32 [P],
     dst2src int32 [P] (= reorder_ids).
+
+    Expert-parallel shard (same page, review of ep_moe/layer.py: with an
+    expert_map the routed ids are translated to this rank's local ids before
+    the preprocess, which then runs over the local experts): expert_map is an
+    int array [E] holding each global expert's local id on this shard, or -1
+    when the expert lives elsewhere.  Reading taken: pairs mapped to -1 are
+    not placed at all (src2dst = -1 for them); the local pairs, P_local of
+    them, are sorted stably by local id, seg_indptr has E_local + 1 entries
+    with E_local = max(expert_map) + 1, and dst2src has length P_local.
     """
     flat = np.asarray(topk_ids, dtype=np.int64).reshape(-1)
     if flat.size and (flat.min() < 0 or flat.max() >= E):
         raise ValueError("expert id out of range")
-    dst2src = np.argsort(flat, kind="stable").astype(np.int32)
-    src2dst = np.empty_like(dst2src)
-    src2dst[dst2src] = np.arange(flat.size, dtype=np.int32)
-    counts = np.bincount(flat, minlength=E)
+    if expert_map is None:
+        local, n_local = flat, E
+    else:
+        emap = np.asarray(expert_map, dtype=np.int64)
+        if emap.shape != (E,) or (emap.size and emap.min() < -1):
+            raise ValueError("expert_map must hold E local ids or -1")
+        n_local = int(emap.max()) + 1 if emap.size else 0
+        local = emap[flat]
+    keep = np.nonzero(local >= 0)[0]
+    dst2src = keep[np.argsort(local[keep], kind="stable")].astype(np.int32)
+    src2dst = np.full(flat.size, -1, dtype=np.int32)
+    src2dst[dst2src] = np.arange(dst2src.size, dtype=np.int32)
+    counts = np.bincount(local[keep], minlength=n_local)
     seg = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
     return seg, src2dst, dst2src
 
@@ -258,13 +276,17 @@ def silu_mul_requant(y13):
 # (6) unpermute and combine
 
 def unpermute_combine(y2, src2dst, topk_w, T: int, k: int) -> np.ndarray:
-    """out[t] = sum_j w[t, j] * y2[src2dst[t*k + j]] in float64 (PR #7762: post-reorder)."""
+    """out[t] = sum_j w[t, j] * y2[src2dst[t*k + j]] in float64 (PR #7762: post-reorder).
+
+    Pairs with src2dst = -1 (routed to another expert-parallel shard) add nothing.
+    """
     y2 = np.asarray(y2, dtype=np.float64)
     w = np.asarray(topk_w, dtype=np.float64).reshape(T, k)
     s2d = np.asarray(src2dst, dtype=np.int64).reshape(T, k)
     out = np.zeros((T, y2.shape[1]), dtype=np.float64)
     for j in range(k):
-        out += w[:, j][:, None] * y2[s2d[:, j]]
+        here = s2d[:, j] >= 0
+        out[here] += w[here, j][:, None] * y2[s2d[here, j]]
     return out
 
 
@@ -272,36 +294,45 @@ def unpermute_combine(y2, src2dst, topk_w, T: int, k: int) -> np.ndarray:
 # the whole layer
 
 def moe_layer(x_bf16, logits, k, w13_of_expert, w13s_of_expert, w2_of_expert, w2s_of_expert,
-              renormalize: bool = True):
+              renormalize: bool = True, expert_map=None):
     """The W4AFP8 MoE layer, step by step; returns a dict of every intermediate.
 
     x_bf16: float array [T, H] holding bf16 values.  w13_of_expert(e) -> int8
     [2I, H] (rows [0, I) gate, [I, 2I) up); w2_of_expert(e) -> int8 [H, I];
-    the *_s functions return fp32 [N, K/128].
+    the *_s functions return fp32 [N, K/128].  With an expert_map (see permute)
+    the layer is one expert-parallel shard: e is a local id, only the pairs
+    routed to local experts are computed, and out_f64 / out are this shard's
+    share of the output (the shards' float64 shares sum to the whole layer's).
     """
     x = np.asarray(x_bf16, dtype=np.float32)
     T = x.shape[0]
     E = np.asarray(logits).shape[1]
     ids, w = route_topk(logits, k, renormalize)
-    seg, src2dst, dst2src = permute(ids, E)
+    seg, src2dst, dst2src = permute(ids, E, expert_map)
     xq, xs = quant_per_token_group(x)
     tok = dst2src.astype(np.int64) // k
     a_codes, a_scales = xq[tok], xs[tok]
+    if dst2src.size == 0:  # no pair routed to this shard
+        return dict(ids=ids, w=w, seg=seg, src2dst=src2dst, dst2src=dst2src, xq=xq, xs=xs, y13=None,
+                    hq=None, hs=None, y2=None, out_f64=np.zeros((T, x.shape[1])), out=np.zeros((T, x.shape[1])))
     y13 = round_bf16(grouped_gemm(a_codes, a_scales, seg, w13_of_expert, w13s_of_expert))
     hq, hs = silu_mul_requant(y13)
     y2 = round_bf16(grouped_gemm(hq, hs, seg, w2_of_expert, w2s_of_expert))
-    out = round_bf16(unpermute_combine(y2, src2dst, w, T, k))
+    out_f64 = unpermute_combine(y2, src2dst, w, T, k)
+    out = round_bf16(out_f64)
     return dict(ids=ids, w=w, seg=seg, src2dst=src2dst, dst2src=dst2src, xq=xq, xs=xs,
-                y13=y13, hq=hq, hs=hs, y2=y2, out=out)
+                y13=y13, hq=hq, hs=hs, y2=y2, out_f64=out_f64, out=out)
 
 
 def moe_tokens(x_bf16_rows, logits_rows, k, w13_of_expert, w13s_of_expert, w2_of_expert,
-               w2s_of_expert, renormalize: bool = True):
+               w2s_of_expert, renormalize: bool = True, expert_map=None):
     """Layer output for a subset of tokens, one routed pair at a time.
 
     Each pair's values do not depend on the other tokens (quantisation is per
     token, the GEMMs are row-wise and the permutation only moves rows), so a
     sample of tokens is computed exactly as moe_layer would for those rows.
+    With an expert_map, the pairs of experts mapped to -1 are skipped and the
+    weight functions take local ids (one expert-parallel shard, as moe_layer).
     Returns out float64 [Ts, H] (bf16 values) and the routing (ids, w).
     """
     x = np.asarray(x_bf16_rows, dtype=np.float32)
@@ -313,6 +344,10 @@ def moe_tokens(x_bf16_rows, logits_rows, k, w13_of_expert, w13s_of_expert, w2_of
         acc = np.zeros(H, dtype=np.float64)
         for j in range(k):
             e = int(ids[t, j])
+            if expert_map is not None:
+                e = int(expert_map[e])
+                if e < 0:
+                    continue
             y13 = round_bf16(w4a8_gemm(xq[t:t + 1], xs[t:t + 1], w13_of_expert(e), w13s_of_expert(e)))
             hq, hs = silu_mul_requant(y13)
             y2 = round_bf16(w4a8_gemm(hq, hs, w2_of_expert(e), w2s_of_expert(e)))

@@ -209,3 +209,52 @@ def test_layer_combining_through_dst2src_is_caught(monkeypatch):
 
     _plant(monkeypatch, "unpermute_combine", wrong_index)
     assert _caught(pm.test_hand_worked_layer) > 0
+
+
+# --- expert-parallel shard mode -------------------------------------------------
+
+import test_oracle_ep as pep  # noqa: E402
+
+
+def test_ep_remote_pairs_kept_are_caught(monkeypatch):
+    good = moe.permute
+
+    def keeps_remote(topk_ids, E, expert_map=None):
+        if expert_map is None:
+            return good(topk_ids, E)
+        return good(topk_ids, E, np.maximum(np.asarray(expert_map), 0))  # remote experts folded into local 0
+
+    _plant(monkeypatch, "permute", keeps_remote)
+    assert _caught(pep.test_permute_ep_hand_worked,
+                   functools.partial(pep.test_shards_add_up_to_the_layer, [[0, 1], [2, 3]])) > 0
+
+
+def test_ep_combine_reading_remote_slots_is_caught(monkeypatch):
+    def no_skip(y2, src2dst, topk_w, T, k):
+        y2 = np.asarray(y2, dtype=np.float64)
+        w = np.asarray(topk_w, dtype=np.float64).reshape(T, k)
+        s2d = np.asarray(src2dst, dtype=np.int64).reshape(T, k)
+        out = np.zeros((T, y2.shape[1]))
+        for j in range(k):
+            out += w[:, j][:, None] * y2[s2d[:, j]]  # -1 reads the last row
+        return out
+
+    _plant(monkeypatch, "unpermute_combine", no_skip)
+    assert _caught(pep.test_combine_skips_remote_pairs,
+                   functools.partial(pep.test_shards_add_up_to_the_layer, [[0, 1], [2, 3]])) > 0
+
+
+def test_ep_unstable_local_order_is_caught(monkeypatch):
+    good = moe.permute
+
+    def unstable(topk_ids, E, expert_map=None):
+        seg, s2d, d2s = good(topk_ids, E, expert_map)
+        d2s = d2s.copy()
+        for e in range(seg.size - 1):
+            d2s[seg[e]:seg[e + 1]] = d2s[seg[e]:seg[e + 1]][::-1]
+        s2d = np.full_like(s2d, -1)
+        s2d[d2s] = np.arange(d2s.size, dtype=s2d.dtype)
+        return seg, s2d, d2s
+
+    _plant(monkeypatch, "permute", unstable)
+    assert _caught(pep.test_permute_ep_hand_worked, pep.test_permute_ep_reordered_local_ids) > 0
