@@ -68,8 +68,13 @@ def workload_desc(name, cfg):
     if name == "linear":
         return f"dense W4AFP8 Linear M={cfg['M']} N={cfg['N']} K={cfg['K']}"
     z = f", router logits + Zipf({cfg['zipf']}) bias" if cfg.get("zipf") else ""
+    ep = ""
+    if cfg.get("ep"):
+        R, r = cfg["ep"]
+        ep = (f"; expert-parallel shard {r} of {R} (experts {r}, {r + R}, ...; only the pairs routed to them, "
+              f"tokens/s counts all T tokens of the shard's call)")
     return (f"{name} MoE layer: T={cfg['T']} H={cfg['H']} I={cfg['I']} E={cfg['E']} top-{cfg['k']}, "
-            f"int4 weights + fp32 scales per 128 K, FP8 E4M3 activations per token per 128{z}")
+            f"int4 weights + fp32 scales per 128 K, FP8 E4M3 activations per token per 128{z}{ep}")
 
 
 def get_workload(spec):
@@ -79,6 +84,11 @@ def get_workload(spec):
     if spec.startswith("moe:"):  # moe:T,H,I,E,k  (custom shape, e.g. small profiling cases)
         T, H, I, E, k = (int(v) for v in spec.split(":")[1].split(","))
         return "moe", dict(T=T, H=H, I=I, E=E, k=k, zipf=None)
+    if spec.startswith("ep:"):  # ep:<workload>:R:r  shard r of R (experts r, r+R, ...) of a named workload
+        _, base, R, r = spec.split(":")
+        cfg = dict(inputs.WORKLOADS[base])
+        cfg["ep"] = (int(R), int(r))
+        return f"ep-{base}", cfg
     return spec, dict(inputs.WORKLOADS[spec])
 
 
@@ -207,6 +217,19 @@ class MoeRunner:
         self.w13s = inputs.gpu_scales(seed, inputs.STREAM_W13_SCALE, (E, H // 128, 2 * I), dev)
         self.w2 = m.w4a8_prepack_weights(inputs.gpu_packed_int4(seed, inputs.STREAM_W2, (E, H, I // 2), dev))
         self.w2s = inputs.gpu_scales(seed, inputs.STREAM_W2_SCALE, (E, I // 128, H), dev)
+        self.ep = cfg.get("ep")
+        self.EL = E
+        self.emap = None
+        if self.ep:  # one expert-parallel shard: experts r, r+R, ... (local ids in that order)
+            R, r = self.ep
+            experts = list(range(r, E, R))
+            idx = torch.tensor(experts, dtype=torch.int64, device=dev)
+            self.w13, self.w13s, self.w2, self.w2s = (t.index_select(0, idx).contiguous()
+                                                      for t in (self.w13, self.w13s, self.w2, self.w2s))
+            emap = np.full(E, -1, np.int32)
+            emap[experts] = np.arange(len(experts), dtype=np.int32)
+            self.emap = torch.from_numpy(emap).to(dev)
+            self.EL = len(experts)
         x_bits = inputs.activations_bf16(seed, T, H)
         logits = inputs.router_logits(seed, T, E, cfg.get("zipf"))
         self.x_pin = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -221,7 +244,7 @@ class MoeRunner:
         L = self.L
         self.p = {n: b + getattr(L, n) for n in ("topk_ids", "topk_w", "seg_indptr", "src2dst", "dst2src",
                                                  "xq", "xs", "xc", "y13", "hq", "hs", "hc", "y2", "permute_ws")}
-        self.permute_ws_bytes = int(m.load().w4a8_workspace_bytes(1, T * k, 0, 0, E))
+        self.permute_ws_bytes = int(m.load().w4a8_workspace_bytes(1, T * k, 0, 0, self.EL))
         self.ld = L.scale_ld
 
     def stages(self, stream):
@@ -230,6 +253,25 @@ class MoeRunner:
         P = T * k
         x, lg, out = self.x.data_ptr(), self.lg.data_ptr(), self.out.data_ptr()
         w13, w13s, w2, w2s = (t.data_ptr() for t in (self.w13, self.w13s, self.w2, self.w2s))
+        if self.ep:  # the seven calls of w4a8_moe_forward_ep
+            EL, emap = self.EL, self.emap.data_ptr()
+            m_dev = p["seg_indptr"] + 8 * EL  # seg_indptr[E_local]: the shard's routed pairs
+            return [
+                ("route", lambda: lib.moe_route_topk(lg, T, E, k, 1, p["topk_ids"], p["topk_w"], stream)),
+                ("permute", lambda: lib.moe_permute_ep(p["topk_ids"], T, k, E, emap, EL, p["seg_indptr"],
+                                                       p["src2dst"], p["dst2src"], p["permute_ws"],
+                                                       self.permute_ws_bytes, stream)),
+                ("quant", lambda: lib.fp8_quant_per_token_group(x, T, H, p["dst2src"], k, P, p["xq"], p["xs"],
+                                                                p["xc"], ld, stream)),
+                ("w13", lambda: lib.w4a8_grouped_gemm(p["xq"], p["xs"], p["xc"], ld, w13, w13s, p["seg_indptr"], EL,
+                                                      2 * I, H, P, p["y13"], None, 0, stream)),
+                ("silu_requant", lambda: lib.silu_mul_requant_rows(p["y13"], P, m_dev, I, p["hq"], p["hs"], p["hc"],
+                                                                   ld, stream)),
+                ("w2", lambda: lib.w4a8_grouped_gemm(p["hq"], p["hs"], p["hc"], ld, w2, w2s, p["seg_indptr"], EL, H,
+                                                     I, P, p["y2"], None, 0, stream)),
+                ("combine", lambda: lib.moe_unpermute_combine(p["y2"], p["src2dst"], p["topk_w"], T, k, H, out,
+                                                              stream)),
+            ]
         return [
             ("route", lambda: lib.moe_route_topk(lg, T, E, k, 1, p["topk_ids"], p["topk_w"], stream)),
             ("permute", lambda: lib.moe_permute(p["topk_ids"], T, k, E, p["seg_indptr"], p["src2dst"],
@@ -249,6 +291,13 @@ class MoeRunner:
         """e2e: pinned host inputs -> device -> whole layer -> pinned host output."""
         self.x.copy_(self.x_pin, non_blocking=True)
         self.lg.copy_(self.lg_pin, non_blocking=True)
+        if self.ep:
+            rc = self.lib.w4a8_moe_forward_ep(self.x.data_ptr(), self.lg.data_ptr(), self.T, self.H, self.I, self.E,
+                                              self.k, 1, self.emap.data_ptr(), self.EL, self.w13.data_ptr(),
+                                              self.w13s.data_ptr(), self.w2.data_ptr(), self.w2s.data_ptr(),
+                                              self.out.data_ptr(), self.ws.data_ptr(), self.ws.numel(), stream)
+            self.out_pin.copy_(self.out, non_blocking=True)
+            return rc
         rc = self.lib.w4a8_moe_forward(self.x.data_ptr(), self.lg.data_ptr(), self.T, self.H, self.I, self.E,
                                        self.k, 1, self.w13.data_ptr(), self.w13s.data_ptr(), self.w2.data_ptr(),
                                        self.w2s.data_ptr(), self.out.data_ptr(), self.ws.data_ptr(),
@@ -258,8 +307,8 @@ class MoeRunner:
 
     def touched_experts(self):
         import torch
-        seg = torch.empty(self.E + 1, dtype=torch.int64)
-        seg.copy_(self.ws[self.L.seg_indptr:self.L.seg_indptr + 8 * (self.E + 1)].view(torch.int64))
+        seg = torch.empty(self.EL + 1, dtype=torch.int64)
+        seg.copy_(self.ws[self.L.seg_indptr:self.L.seg_indptr + 8 * (self.EL + 1)].view(torch.int64))
         s = seg.numpy()
         return int(np.count_nonzero(np.diff(s))), s
 
@@ -332,7 +381,7 @@ def run_ours(args, name, cfg):
                 for j, (nm, _) in enumerate(st)}
     ms = reduce_max(ms, dev)
     T, H, I, E, k = r.T, r.H, r.I, r.E, r.k
-    P = T * k
+    P = int(seg[-1])  # routed pairs computed (all T*k, or the shard's)
     ms_step = ms / K
     value = throughput(T * K, world, ms)
     flops = 2.0 * P * (2 * I * H + I * H)
@@ -385,7 +434,7 @@ def run_ours(args, name, cfg):
     if not args.no_e2e:
         res["e2e"] = e2e_moe(r, args, dev, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(name, args)
+        res["cpu_baseline"] = cpu_baseline(name, args.workload, args)
     if world > 1:
         dist.destroy_process_group()
     if rank == 0:
@@ -492,17 +541,25 @@ def oracle_sample(name, cfg, seed, n_tokens):
     sel = np.arange(n_tokens)
     # weights are model parameters already in memory: generate them before timing
     ids, _ = oracle.route_topk(logits[sel], cfg["k"])
-    cache13 = {int(e): (w13.w(e), w13.s(e)) for e in np.unique(ids)}
-    cache2 = {int(e): (w2.w(e), w2.s(e)) for e in np.unique(ids)}
+    emap, glob = None, np.arange(cfg["E"])
+    if cfg.get("ep"):  # one expert-parallel shard: local id l is global expert r + l*R
+        R, r = cfg["ep"]
+        glob = np.arange(r, cfg["E"], R)
+        emap = np.full(cfg["E"], -1, np.int64)
+        emap[glob] = np.arange(glob.size)
+    used = [int(e) for e in np.unique(ids) if emap is None or emap[e] >= 0]
+    loc = {(int(emap[e]) if emap is not None else e): e for e in used}
+    cache13 = {l: (w13.w(e), w13.s(e)) for l, e in loc.items()}
+    cache2 = {l: (w2.w(e), w2.s(e)) for l, e in loc.items()}
 
     def run():
         return oracle.moe_tokens(x[sel], logits[sel], cfg["k"], lambda e: cache13[e][0], lambda e: cache13[e][1],
-                                 lambda e: cache2[e][0], lambda e: cache2[e][1])
+                                 lambda e: cache2[e][0], lambda e: cache2[e][1], expert_map=emap)
     return run
 
 
 def default_cpu_tokens(name):
-    return {"tiny": 64, "decode": 1, "prefill": 1, "skewed": 1}.get(name, 1)
+    return {"tiny": 64, "decode": 1, "prefill": 1, "skewed": 1}.get(name, 8 if name.startswith("ep-") else 1)
 
 
 def run_reference(args, name, cfg):
@@ -528,16 +585,17 @@ def run_reference(args, name, cfg):
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {"workload": workload_desc(name, cfg)},
            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                            "sample": f"{n} token(s) of the workload per step ({n * cfg['k']} routed pairs), "
+                            "sample": f"{n} token(s) of the workload per step ({n * cfg['k']} routed pairs"
+                                      f"{', those of the shard computed' if cfg.get('ep') else ''}), "
                                       f"numpy float64, one BLAS thread"},
            "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
 
 
-def cpu_baseline(name, args):
+def cpu_baseline(name, spec, args):
     """The oracle in a single-threaded child process on a bounded sample (~10-30 s)."""
-    n = {"tiny": 64}.get(name, 4)
-    cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--workload", name, "--steps", "1",
+    n = {"tiny": 64}.get(name, 32 if name.startswith("ep-") else 4)
+    cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--workload", spec, "--steps", "1",
            "--warmup", "0", "--cpu-tokens", str(n), "--seed", str(args.seed)]
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
     for v in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):

@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define W4A8MOE_ABI_VERSION 2
+#define W4A8MOE_ABI_VERSION 3
 
 typedef enum {
   W4A8_OK = 0,
@@ -108,6 +108,26 @@ int moe_permute(const int32_t* topk_ids, int64_t T, int k, int64_t E, int64_t* s
                 int32_t* src2dst, int32_t* dst2src, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * (2') The same preprocess for one expert-parallel shard (PR #7762 page,
+ * review of ep_moe/layer.py: with an expert_map the routed ids are translated
+ * to local ids before the preprocess, which then runs over the local experts).
+ *   expert_map int32 [E] (device): local id in [0, E_local) of each global
+ *     expert held by this shard, -1 for an expert held elsewhere; NULL means
+ *     the identity (then E_local must equal E and this is moe_permute).
+ *   seg_indptr int64 [E_local+1]: segments of the local experts; seg_indptr[E_local]
+ *     = P_local, the number of pairs routed to local experts (device side only).
+ *   src2dst int32 [T*k]: sorted position of pair f, or -1 when its expert is remote.
+ *   dst2src int32 [T*k]: the local pairs at [0, P_local), -1 from P_local on.
+ * Local pairs are ordered by local id, and within one by ascending f.  Routed
+ * ids outside [0, E) or map entries outside [-1, E_local) set the device error
+ * word (code 2) and those pairs are left out.  1 <= E_local <= 1024.
+ * ws / ws_bytes: w4a8_workspace_bytes(W4A8_OP_PERMUTE, T*k, 0, 0, E_local).
+ */
+int moe_permute_ep(const int32_t* topk_ids, int64_t T, int k, int64_t E, const int32_t* expert_map,
+                   int64_t E_local, int64_t* seg_indptr, int32_t* src2dst, int32_t* dst2src, void* ws,
+                   size_t ws_bytes, void* stream);
+
+/*
  * (3) FP8 E4M3 activation quantisation per token per group of 128 columns
  * ("scale operations on the input hidden states", PR #7762 page, Cutlass W4A8
  * MoE): amax = max|x| over the group, clamped to >= 1e-12 (DeepGEMM PR #53
@@ -118,6 +138,8 @@ int moe_permute(const int32_t* topk_ids, int64_t T, int k, int64_t E, int64_t* s
  * row_index = NULL output row j reads input row j and M_out must equal M_src.
  * In the MoE this quantises the permuted copy directly (row_index = dst2src,
  * row_div = k); quantisation is per row, so it equals permuting quantised rows.
+ * Output rows whose row_index is negative (the -1 tail of an expert-parallel
+ * shard's dst2src) are skipped: q, scales and gcorr keep their old contents.
  *   x bf16 [M_src][K]   q uint8 [M_out][K]   scales, gcorr fp32 [K/128][scale_ld]
  *   K % 128 == 0, scale_ld >= M_out, scale_ld % 4 == 0.  gcorr may be NULL.
  *   x 16-byte aligned, q 8-byte aligned, scales and gcorr 4-byte aligned.
@@ -168,9 +190,19 @@ int silu_mul_requant(const uint16_t* gate_up, int64_t M, int64_t I, uint8_t* q, 
                      float* gcorr, int64_t scale_ld, void* stream);
 
 /*
+ * (5') The same over the rows [0, min(M, *m_dev)) only: m_dev (device, int64;
+ * NULL = all M rows) is a row count known only on the device, such as
+ * seg_indptr[E_local] of an expert-parallel shard (the pairs routed to the
+ * shard's experts).  Rows past it are left unwritten.
+ */
+int silu_mul_requant_rows(const uint16_t* gate_up, int64_t M, const int64_t* m_dev, int64_t I, uint8_t* q,
+                          float* scales, float* gcorr, int64_t scale_ld, void* stream);
+
+/*
  * (6) Unpermute and combine (PR #7762 page: post-reordering of the outputs):
  *   out[t][c] = bf16( sum_{j=0..k-1} topk_w[t][j] * Y[src2dst[t*k+j]][c] ),
- * fp32 accumulation in j order.
+ * fp32 accumulation in j order.  Slots with src2dst = -1 (pairs of another
+ * expert-parallel shard) add nothing; a token with none left gets zeros.
  *   Y bf16 [T*k][H]   src2dst int32 [T*k]   topk_w fp32 [T][k]   out bf16 [T][H]
  *   H % 8 == 0.
  */
@@ -214,6 +246,24 @@ int w4a8_moe_forward(const uint16_t* x, const float* logits, int64_t T, int64_t 
                      const uint8_t* w2, const float* w2_s, uint16_t* out, void* ws,
                      size_t ws_bytes, void* stream);
 size_t w4a8_moe_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int k);
+
+/*
+ * One expert-parallel shard of the layer (PR #7762 page, ep-moe mode and the
+ * expert_map review of ep_moe/layer.py): routing over all E experts, then
+ * (2') with expert_map, and the rest over the pairs routed to this shard's
+ * E_local experts only.  out is this shard's share of the layer output (the
+ * sum over the shards' shares, taken outside this call, is the layer).
+ *   logits fp32 [T][E]   expert_map int32 [E] (device; see moe_permute_ep)
+ *   w13, w13_s, w2, w2_s: the E_local local experts, laid out as in
+ *   w4a8_moe_forward with E_local in place of E.  1 <= E_local <= E.
+ *   ws: w4a8_moe_workspace_bytes(T, H, I, E, k) bytes (the same layout).
+ * The row count P_local stays on the device: quantisation, SiLU and the
+ * GEMMs read it from seg_indptr, so no host synchronisation is added.
+ */
+int w4a8_moe_forward_ep(const uint16_t* x, const float* logits, int64_t T, int64_t H, int64_t I,
+                        int64_t E, int k, int renormalize, const int32_t* expert_map, int64_t E_local,
+                        const uint8_t* w13, const float* w13_s, const uint8_t* w2, const float* w2_s,
+                        uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * w4a8_moe_forward without a workspace: for callers that cannot allocate

@@ -30,14 +30,14 @@ def test_every_declared_symbol_is_exported(clib):
     assert len(names) >= 16
     for n in ["moe_route_topk", "moe_permute", "fp8_quant_per_token_group", "w4a8_grouped_gemm",
               "silu_mul_requant", "moe_unpermute_combine", "w4a8_linear", "w4a8_prepack_weights",
-              "w4a8_moe_forward", "w4a8_moe_forward_noalloc"]:
+              "w4a8_moe_forward", "w4a8_moe_forward_noalloc", "moe_permute_ep", "w4a8_moe_forward_ep"]:
         assert n in names
     for n in names:
         assert hasattr(clib, n), n
 
 
 def test_status_strings_and_version(clib):
-    assert clib.w4a8_abi_version() == 2
+    assert clib.w4a8_abi_version() == 3
     assert clib.w4a8_status_string(0) == b"ok"
     assert clib.w4a8_status_string(1) == b"invalid argument"
     assert clib.w4a8_status_string(4) == b"device-side wait timed out"
@@ -52,6 +52,9 @@ P16 = ctypes.c_void_p(16)  # a 16-byte aligned non-null dummy (never dereference
     (lambda L: L.moe_route_topk(P16, 4, 2000, 2, 1, P16, P16, NULL), b"E=2000"),
     (lambda L: L.moe_permute(P16, 4, 2, 0, P16, P16, P16, NULL, 0, NULL), b"E=0"),
     (lambda L: L.moe_permute(P16, 1024, 8, 256, P16, P16, P16, NULL, 0, NULL), b"workspace"),
+    (lambda L: L.moe_permute_ep(P16, 4, 2, 8, NULL, 4, P16, P16, P16, NULL, 0, NULL), b"expert_map"),
+    (lambda L: L.moe_permute_ep(P16, 4, 2, 8, P16, 0, P16, P16, P16, NULL, 0, NULL), b"E_local=0"),
+    (lambda L: L.moe_permute_ep(P16, 1024, 8, 256, P16, 32, P16, P16, P16, NULL, 0, NULL), b"workspace"),
     (lambda L: L.fp8_quant_per_token_group(P16, 4, 100, NULL, 1, 4, P16, P16, NULL, 4, NULL), b"K=100"),
     (lambda L: L.fp8_quant_per_token_group(P16, 4, 128, NULL, 1, 4, P16, P16, NULL, 2, NULL), b"scale_ld"),
     (lambda L: L.w4a8_grouped_gemm(P16, P16, P16, 4, P16, P16, P16, 2, 256, 200, 4, P16, NULL, 0, NULL), b"K=200"),
@@ -62,12 +65,17 @@ P16 = ctypes.c_void_p(16)  # a 16-byte aligned non-null dummy (never dereference
     (lambda L: L.w4a8_linear(P16, P16, ctypes.c_void_p(20), 4, P16, P16, 4, 128, 256, P16, NULL, 0, NULL),
      b"aligned"),
     (lambda L: L.silu_mul_requant(P16, 4, 100, P16, P16, NULL, 4, NULL), b"I=100"),
+    (lambda L: L.silu_mul_requant_rows(P16, 4, P16, 100, P16, P16, NULL, 4, NULL), b"I=100"),
     (lambda L: L.moe_unpermute_combine(P16, P16, P16, 4, 2, 12, P16, NULL), b"H=12"),
     (lambda L: L.w4a8_prepack_weights(P16, 4, 12, P16, NULL), b"K=12"),
     (lambda L: L.w4a8_moe_forward(P16, P16, 4, 256, 256, 8, 2, 1, P16, P16, P16, P16, P16, P16, 10, NULL),
      b"workspace too small"),
     (lambda L: L.w4a8_moe_forward_noalloc(P16, P16, 4096, 7168, 2048, 8, 8, 1, P16, P16, P16, P16, P16, NULL),
      b"at most"),
+    (lambda L: L.w4a8_moe_forward_ep(P16, P16, 4, 256, 256, 8, 2, 1, P16, 9, P16, P16, P16, P16, P16, P16,
+                                     1 << 30, NULL), b"E_local=9"),
+    (lambda L: L.w4a8_moe_forward_ep(P16, P16, 4, 256, 256, 8, 2, 1, NULL, 4, P16, P16, P16, P16, P16, P16,
+                                     1 << 30, NULL), b"expert_map"),
 ])
 def test_host_validation_rejects_before_launch(clib, call, msg):
     assert call(clib) == 1  # W4A8_ERR_INVALID_ARG

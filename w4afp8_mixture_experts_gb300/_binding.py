@@ -26,12 +26,15 @@ _SIGS = {
     "w4a8_device_error": (_c_int, []),
     "moe_route_topk": (_c_int, [_c_vp, _c_i64, _c_i64, _c_int, _c_int, _c_vp, _c_vp, _c_vp]),
     "moe_permute": (_c_int, [_c_vp, _c_i64, _c_int, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]),
+    "moe_permute_ep": (_c_int, [_c_vp, _c_i64, _c_int, _c_i64, _c_vp, _c_i64, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz,
+                                _c_vp]),
     "fp8_quant_per_token_group": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp,
                                            _c_i64, _c_vp]),
     "w4a8_grouped_gemm": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64,
                                    _c_i64, _c_vp, _c_vp, _c_sz, _c_vp]),
     "w4a8_prepack_weights": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_vp]),
     "silu_mul_requant": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64, _c_vp]),
+    "silu_mul_requant_rows": (_c_int, [_c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64, _c_vp]),
     "moe_unpermute_combine": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_int, _c_i64, _c_vp, _c_vp]),
     "w4a8_linear": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp,
                              _c_sz, _c_vp]),
@@ -39,6 +42,8 @@ _SIGS = {
     "w4a8_moe_forward": (_c_int, [_c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_vp,
                                   _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]),
     "w4a8_moe_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_i64, _c_i64, _c_int]),
+    "w4a8_moe_forward_ep": (_c_int, [_c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_vp, _c_i64,
+                                     _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]),
     "w4a8_moe_forward_noalloc": (_c_int, [_c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_vp,
                                           _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
     "w4a8_moe_noalloc_scratch_bytes": (_c_sz, []),
@@ -131,6 +136,23 @@ def moe_permute(topk_ids, E: int):
     need = int(load().w4a8_workspace_bytes(1, T * k, 0, 0, E))
     ws = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
     _check(load().moe_permute(_p(topk_ids), T, k, E, _p(seg), _p(s2d), _p(d2s), _p(ws), need, _stream()))
+    return seg, s2d, d2s
+
+
+def moe_permute_ep(topk_ids, E: int, expert_map, E_local: int):
+    """One expert-parallel shard's permutation: expert_map int32 [E] (local id or -1).
+    Returns (seg_indptr int64 [E_local+1], src2dst int32 [T*k], dst2src int32 [T*k])."""
+    _req(topk_ids, torch.int32, "topk_ids", 2)
+    _req(expert_map, torch.int32, "expert_map", 1)
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    seg = torch.empty(E_local + 1, dtype=torch.int64, device=dev)
+    s2d = torch.empty(T * k, dtype=torch.int32, device=dev)
+    d2s = torch.empty(T * k, dtype=torch.int32, device=dev)
+    need = int(load().w4a8_workspace_bytes(1, T * k, 0, 0, E_local))
+    ws = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
+    _check(load().moe_permute_ep(_p(topk_ids), T, k, E, _p(expert_map), E_local, _p(seg), _p(s2d), _p(d2s), _p(ws),
+                                 need, _stream()))
     return seg, s2d, d2s
 
 
@@ -252,6 +274,33 @@ def w4a8_moe_forward(x, logits, k: int, w13, w13_s, w2, w2_s, renormalize: bool 
         out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
     _check(load().w4a8_moe_forward(_p(x), _p(logits), T, H, I, E, k, int(bool(renormalize)), _p(w13), _p(w13_s),
                                    _p(w2), _p(w2_s), _p(out), _p(ws), ws.numel(), _stream()))
+    return out
+
+
+def w4a8_moe_forward_ep(x, logits, k: int, expert_map, w13, w13_s, w2, w2_s, renormalize: bool = True, ws=None,
+                        out=None):
+    """One expert-parallel shard of the layer: routing over the E = logits.shape[1] experts, the rest over
+    the E_local = w13.shape[0] local experts named by expert_map (int32 [E], local id or -1).  Returns
+    this shard's share of the layer output, bf16 [T, H]."""
+    _req(x, torch.bfloat16, "x", 2)
+    _req(logits, torch.float32, "logits", 2)
+    _req(expert_map, torch.int32, "expert_map", 1)
+    _req(w13, torch.uint8, "w13", 3)
+    _req(w2, torch.uint8, "w2", 3)
+    _req(w13_s, torch.float32, "w13_s", 3)
+    _req(w2_s, torch.float32, "w2_s", 3)
+    T, H = x.shape
+    E = logits.shape[1]
+    E_local = w13.shape[0]
+    I = w13.shape[1] // 2
+    need = int(load().w4a8_moe_workspace_bytes(T, H, I, E, k))
+    if ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _check(load().w4a8_moe_forward_ep(_p(x), _p(logits), T, H, I, E, k, int(bool(renormalize)), _p(expert_map),
+                                      E_local, _p(w13), _p(w13_s), _p(w2), _p(w2_s), _p(out), _p(ws), ws.numel(),
+                                      _stream()))
     return out
 
 

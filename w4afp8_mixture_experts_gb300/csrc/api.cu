@@ -161,3 +161,46 @@ extern "C" int w4a8_moe_forward(const uint16_t* x, const float* logits, int64_t 
     return rc;
   return moe_unpermute_combine(y2, s2d, tw, T, k, H, out, stream);
 }
+
+extern "C" int w4a8_moe_forward_ep(const uint16_t* x, const float* logits, int64_t T, int64_t H, int64_t I,
+                                   int64_t E, int k, int renormalize, const int32_t* expert_map, int64_t E_local,
+                                   const uint8_t* w13, const float* w13_s, const uint8_t* w2, const float* w2_s,
+                                   uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+  using namespace w4a8;
+  w4a8_moe_layout L;
+  int rc = layout_of(T, H, I, E, k, &L);
+  if (rc) return rc;
+  W4A8_REQUIRE(expert_map != nullptr, "expert_map is null");
+  W4A8_REQUIRE(E_local >= 1 && E_local <= E && E_local <= 1024, "E_local=%lld must be in [1, min(E, 1024)]",
+               (long long)E_local);
+  W4A8_REQUIRE(ws != nullptr && ws_bytes >= L.total, "workspace too small: need %zu bytes", L.total);
+  W4A8_REQUIRE((reinterpret_cast<uintptr_t>(ws) & 255) == 0, "workspace must be 256-byte aligned");
+  if (T == 0) return W4A8_OK;
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  int32_t* ids = reinterpret_cast<int32_t*>(b + L.topk_ids);
+  float* tw = reinterpret_cast<float*>(b + L.topk_w);
+  int64_t* seg = reinterpret_cast<int64_t*>(b + L.seg_indptr);  // [E_local + 1] of the [E + 1] slot
+  int32_t* s2d = reinterpret_cast<int32_t*>(b + L.src2dst);
+  int32_t* d2s = reinterpret_cast<int32_t*>(b + L.dst2src);
+  uint8_t* xq = b + L.xq;
+  float* xs = reinterpret_cast<float*>(b + L.xs);
+  float* xc = reinterpret_cast<float*>(b + L.xc);
+  uint16_t* y13 = reinterpret_cast<uint16_t*>(b + L.y13);
+  uint8_t* hq = b + L.hq;
+  float* hs = reinterpret_cast<float*>(b + L.hs);
+  float* hc = reinterpret_cast<float*>(b + L.hc);
+  uint16_t* y2 = reinterpret_cast<uint16_t*>(b + L.y2);
+  const int64_t P = T * k;  // upper bound of the local pairs; the count itself is seg[E_local]
+  if ((rc = moe_route_topk(logits, T, E, k, renormalize, ids, tw, stream))) return rc;
+  if ((rc = moe_permute_ep(ids, T, k, E, expert_map, E_local, seg, s2d, d2s, b + L.permute_ws,
+                           permute_ws_bytes(P, E_local), stream)))
+    return rc;
+  if ((rc = fp8_quant_per_token_group(x, T, H, d2s, k, P, xq, xs, xc, L.scale_ld, stream))) return rc;
+  if ((rc = w4a8_grouped_gemm(xq, xs, xc, L.scale_ld, w13, w13_s, seg, E_local, 2 * I, H, P, y13, nullptr, 0,
+                              stream)))
+    return rc;
+  if ((rc = silu_mul_requant_rows(y13, P, seg + E_local, I, hq, hs, hc, L.scale_ld, stream))) return rc;
+  if ((rc = w4a8_grouped_gemm(hq, hs, hc, L.scale_ld, w2, w2_s, seg, E_local, H, I, P, y2, nullptr, 0, stream)))
+    return rc;
+  return moe_unpermute_combine(y2, s2d, tw, T, k, H, out, stream);
+}

@@ -1,5 +1,6 @@
 // Unpermute and combine (SGLang PR #7762 page: post-reordering of the outputs):
-// out[t][c] = bf16( sum_j topk_w[t][j] * Y[src2dst[t*k+j]][c] ), fp32 in j order.
+// out[t][c] = bf16( sum_j topk_w[t][j] * Y[src2dst[t*k+j]][c] ), fp32 in j order; slots with
+// src2dst = -1 (routed to another expert-parallel shard) add nothing.
 // CTA per token (and, for few tokens, per slice of 2048 columns); each thread loads the k rows' 8 bf16 of its
 // columns with 16-byte loads.
 #include "common.cuh"
@@ -14,21 +15,30 @@ __global__ void __launch_bounds__(kThreads)
                    int k, int64_t H, uint16_t* __restrict__ out) {
   __shared__ int64_t rows[32];
   __shared__ float ws[32];
+  __shared__ int n_here;
   pdl_trigger();
   pdl_wait();
   const int64_t t = blockIdx.x;
-  if (threadIdx.x < k) {
-    rows[threadIdx.x] = static_cast<int64_t>(s2d[t * k + threadIdx.x]) * H;
-    ws[threadIdx.x] = w[t * k + threadIdx.x];
+  if (threadIdx.x < 32) {  // the token's placed pairs in slot order (src2dst = -1: another shard's expert)
+    const int j = threadIdx.x;
+    const int d = j < k ? s2d[t * k + j] : -1;
+    const unsigned here = __ballot_sync(0xffffffffu, d >= 0);
+    if (d >= 0) {
+      const int pos = __popc(here & ((1u << j) - 1u));
+      rows[pos] = static_cast<int64_t>(d) * H;
+      ws[pos] = w[t * k + j];
+    }
+    if (j == 0) n_here = __popc(here);
   }
   __syncthreads();
+  const int kh = n_here;
   for (int64_t c = (static_cast<int64_t>(blockIdx.y) * kThreads + threadIdx.x) * 8; c < H;
        c += static_cast<int64_t>(gridDim.y) * kThreads * 8) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll 8
-    for (int j = 0; j < k; ++j) {
+    for (int j = 0; j < kh; ++j) {
       const uint4 v = *reinterpret_cast<const uint4*>(Y + rows[j] + c);
       const float wj = ws[j];
       const uint32_t u[4] = {v.x, v.y, v.z, v.w};

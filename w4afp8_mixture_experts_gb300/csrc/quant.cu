@@ -60,7 +60,9 @@ __global__ void __launch_bounds__(256)
   if (task >= M_out * G) return;
   const int64_t row = task / G;
   const int64_t g = task - row * G;
-  const int64_t src = row_index ? static_cast<int64_t>(row_index[row]) / row_div : row;
+  const int64_t ri = row_index ? static_cast<int64_t>(row_index[row]) : row;
+  if (ri < 0) return;  // no source row (a pair of a remote expert): left unwritten; the group's lanes leave together
+  const int64_t src = row_index ? ri / row_div : row;
   const uint4* xp = reinterpret_cast<const uint4*>(x + src * K + g * kGroup + sub * kQuantVals);
   uint32_t w[kQuantVals / 2];
   uint32_t mx = 0;
@@ -122,8 +124,8 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 // lane computes its 32 values of h = silu(gate) * up into registers, then quantises them.
 template <int LANES>
 __global__ void __launch_bounds__(256)
-    silu_quad_kernel(const uint16_t* __restrict__ gu, int64_t M, int64_t I, uint8_t* __restrict__ q,
-                     float* __restrict__ scales, float* __restrict__ gcorr, int64_t ld) {
+    silu_quad_kernel(const uint16_t* __restrict__ gu, int64_t M, const int64_t* __restrict__ m_dev, int64_t I,
+                     uint8_t* __restrict__ q, float* __restrict__ scales, float* __restrict__ gcorr, int64_t ld) {
   constexpr int kQuantVals = kGroup / LANES;  // values per lane
   pdl_trigger();
   pdl_wait();
@@ -133,6 +135,7 @@ __global__ void __launch_bounds__(256)
   const int sub = static_cast<int>(tid % LANES);
   if (task >= M * G) return;  // a group's lanes leave together
   const int64_t row = task / G;
+  if (m_dev && row >= *m_dev) return;  // rows past the device-side count are not produced
   const int64_t g = task - row * G;
   const uint4* gp = reinterpret_cast<const uint4*>(gu + row * 2 * I + g * kGroup + sub * kQuantVals);
   const uint4* up = reinterpret_cast<const uint4*>(gu + row * 2 * I + I + g * kGroup + sub * kQuantVals);
@@ -212,8 +215,8 @@ extern "C" int fp8_quant_per_token_group(const uint16_t* x, int64_t M_src, int64
                     row_index, row_div, M_out, q, scales, gcorr, scale_ld);
 }
 
-extern "C" int silu_mul_requant(const uint16_t* gate_up, int64_t M, int64_t I, uint8_t* q, float* scales,
-                                float* gcorr, int64_t scale_ld, void* stream) {
+extern "C" int silu_mul_requant_rows(const uint16_t* gate_up, int64_t M, const int64_t* m_dev, int64_t I,
+                                     uint8_t* q, float* scales, float* gcorr, int64_t scale_ld, void* stream) {
   using namespace w4a8;
   W4A8_REQUIRE(I > 0 && I % kGroup == 0, "I=%lld must be a positive multiple of 128", (long long)I);
   W4A8_REQUIRE(M >= 0, "negative row count");
@@ -229,5 +232,10 @@ extern "C" int silu_mul_requant(const uint16_t* gate_up, int64_t M, int64_t I, u
   W4A8_REQUIRE(blocks < (1ll << 31), "too many rows");
   return launch_pdl("silu_quad_kernel", small ? silu_quad_kernel<16> : silu_quad_kernel<4>,
                     dim3(static_cast<unsigned>(blocks)), dim3(256), 0, static_cast<cudaStream_t>(stream), gate_up, M,
-                    I, q, scales, gcorr, scale_ld);
+                    m_dev, I, q, scales, gcorr, scale_ld);
+}
+
+extern "C" int silu_mul_requant(const uint16_t* gate_up, int64_t M, int64_t I, uint8_t* q, float* scales,
+                                float* gcorr, int64_t scale_ld, void* stream) {
+  return silu_mul_requant_rows(gate_up, M, nullptr, I, q, scales, gcorr, scale_ld, stream);
 }
