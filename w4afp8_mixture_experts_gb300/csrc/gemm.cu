@@ -59,6 +59,7 @@ constexpr int kWarpTmaAct = 1;               // producer of the token and scale 
 constexpr int kWarpMma = 2;                  // warps 2 .. 1 + kMmaWarps issue the MMAs
 constexpr int kConvWarps = 4;                // converter warps per set: one per tensor-memory lane quarter
 constexpr int kMaxExperts = 1024;
+constexpr int kMaxDynSmem = 227 * 1024;  // dynamic shared memory a CTA may use on sm_100 / sm_103
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s: no legitimate wait comes close
 
 __device__ unsigned int g_gemm_error;
@@ -108,8 +109,8 @@ struct Cfg {
   static constexpr int kNumBars = 2 * STAGES + 2 * TSTAGES + 2 * SSTAGES + 2 * ABUF + 2 * NP + 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffSched = kOffMisc + 64;
-  static constexpr int kSmemBytesMax = kOffSched + 2 * (kMaxExperts + 1) * 4 + 1024;
-  static int smem_bytes(int E) { return kOffSched + 2 * (E + 1) * 4 + 1024; }
+  // schedule: [E+1] chunk prefix, [E+1] row starts, [cap] int16 expert of each chunk (cap may be 0)
+  static int smem_bytes(int E, int cap) { return kOffSched + 2 * (E + 1) * 4 + 2 * cap + 16 + 1024; }
   // tensor memory: [NP][GPS][NMAX] partials | [ABUF][GPS][32] converted weights (A_TMEM) |
   // with two epilogue sets, two NMAX-column slots (by tile parity) through which set 1 hands
   // its accumulators to set 0 at the end of a tile
@@ -142,9 +143,9 @@ struct Cfg {
   static constexpr int kMmaCommits = kMmaByStage ? 1 : MMAS_;
   static_assert(!kMmaByStage || (TSTAGES_ % MMAS_ == 0 && ABUF_ % MMAS_ == 0),
                 "stage-wise MMA warps: token and A ring depths must be multiples of the MMA warps");
-  static constexpr int kRegsCtl = 64;    // warps 0-3: the two producers and the MMA warps
+  static constexpr int kRegsCtl = 72;    // warps 0-3: the two producers and the MMA warps
   static constexpr int kRegsConv = 96;   // converter warpgroups
-  static constexpr int kRegsEpi = 176;   // epilogue warpgroups
+  static constexpr int kRegsEpi = 168;   // epilogue warpgroups
   static_assert(!kRegSplit || (kThreads == 512 && kWarpConv0 == 4 && kWarpEpi0 % 4 == 0),
                 "register split: warp roles aligned to warpgroups, 512 threads");
   static_assert(!kRegSplit || 128 * kRegsCtl + 32 * kConvSets * kConvWarps * kRegsConv + 32 * EPIW_ * kRegsEpi <=
@@ -159,6 +160,7 @@ struct GemmParams {
   int E, N, K, M;      // M: rows of A (dense) / M_total
   int gps;             // 128-K groups per stage (divides K/128, <= Cfg::GPS)
   int splits;          // K splits per tile (1: none)
+  int chunk_cap;       // entries of the chunk -> expert table in shared memory (0: binary search)
 };
 
 // UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -212,6 +214,7 @@ __global__ void __launch_bounds__(256) prepack_kernel(const uint32_t* __restrict
 struct Sched {
   const int* prefix;  // [E+1] chunk prefix
   const int* start;   // [E+1] row starts
+  const int16_t* chunk_e;  // [chunks] expert of each chunk, or nullptr (binary search over prefix)
   int E, NMAX, nblk;
   int S, Gs, gps;     // K splits per tile, stages per tile, groups per stage
   // item = tile * S + split; split s covers stages [s*Gs/S, (s+1)*Gs/S) of the tile
@@ -224,12 +227,16 @@ struct Sched {
     const int item = item_ / S;
     const int chunk = item / nblk;
     nb = item - chunk * nblk;
-    int lo = 0, hi = E;  // prefix[lo] <= chunk < prefix[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (prefix[mid] <= chunk) lo = mid; else hi = mid;
+    if (chunk_e) {
+      e = chunk_e[chunk];
+    } else {
+      int lo = 0, hi = E;  // prefix[lo] <= chunk < prefix[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= chunk) lo = mid; else hi = mid;
+      }
+      e = lo;
     }
-    e = lo;
     // chunks sit on a grid of NMAX rows from the expert's first row rounded down to 4, so a
     // tile's token rows start 4-aligned (16-byte scale vectors) and only the first one is ragged
     const int st = start[e], end = start[e + 1];
@@ -334,6 +341,7 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
   const int E = prm.seg ? prm.E : 1;
   int* s_prefix = reinterpret_cast<int*>(smem + CF::kOffSched);  // [E+1]
   int* s_start = s_prefix + (E + 1);                              // [E+1]
+  int16_t* s_chunk_e = reinterpret_cast<int16_t*>(s_start + (E + 1));  // [chunk_cap]
 
   pdl_trigger();  // the next kernel may launch once every CTA has started (it waits for this grid)
   const int warp = threadIdx.x >> 5;
@@ -415,10 +423,20 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
   __syncthreads();
   tc_fence_after();
 
+  // chunk -> expert table: every role decodes each of its tiles, and a binary search over the
+  // experts is a chain of dependent shared-memory loads (~1500 cycles per tile under load)
+  const int n_chunks = s_prefix[E];
+  const bool table = n_chunks <= prm.chunk_cap;
+  if (table) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+      for (int c = s_prefix[e]; c < s_prefix[e + 1]; ++c) s_chunk_e[c] = static_cast<int16_t>(e);
+  }
+  __syncthreads();
+
   const uint32_t tmem_base = *s_tmem;
   const int S = SPLIT ? prm.splits : 1;  // 1 folds the split arithmetic away
-  Sched sch{s_prefix, s_start, E, NMAX, nblk, S, G / gps, gps};
-  const int n_items = s_prefix[E] * nblk * S;
+  Sched sch{s_prefix, s_start, table ? s_chunk_e : nullptr, E, NMAX, nblk, S, G / gps, gps};
+  const int n_items = n_chunks * nblk * S;
 
   // Counters: `it` counts 128-K groups, `st` counts stages of gps groups; stage st holds
   // groups [st*gps, st*gps + gps) of one tile (gps divides K/128, so stages never straddle
@@ -985,9 +1003,9 @@ int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, c
   static bool attr_set = false;  // per template instance
   if (!attr_set) {
     if (cudaFuncSetAttribute(w4a8_gemm_kernel<CF, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             CF::kSmemBytesMax) != cudaSuccess ||
+                             kMaxDynSmem) != cudaSuccess ||
         cudaFuncSetAttribute(w4a8_gemm_kernel<CF, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             CF::kSmemBytesMax) != cudaSuccess)
+                             kMaxDynSmem) != cudaSuccess)
       return check_launch("cudaFuncSetAttribute(gemm)");
     if constexpr (CF::kRegSplit) {
       // setmaxnreg.inc waits until the released registers cover the request: the warpgroups'
@@ -1016,8 +1034,14 @@ int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, c
   p.gps = gps;
   p.partial = partial;
   p.splits = splits;
+  // chunk -> expert table: an expert's chunks sit on the NMAX grid from its first row rounded down to
+  // 4, so it has at most (3 + rows) / NMAX + 1 of them
+  const int Ed = seg ? static_cast<int>(E) : 1;
+  const int64_t bound = seg ? (3 * E + M) / CF::NMAX + E + 1 : (M + CF::NMAX - 1) / CF::NMAX + 1;
+  const int64_t room = (kMaxDynSmem - CF::smem_bytes(Ed, 0)) / 2;
+  p.chunk_cap = static_cast<int>(std::max<int64_t>(0, std::min(bound, room)));
   return launch_pdl("w4a8_gemm_kernel", splits > 1 ? w4a8_gemm_kernel<CF, true> : w4a8_gemm_kernel<CF, false>,
-                    dim3(num_sms()), dim3(CF::kThreads), CF::smem_bytes(static_cast<int>(seg ? E : 1)), st, tA, tAS,
+                    dim3(num_sms()), dim3(CF::kThreads), CF::smem_bytes(Ed, p.chunk_cap), st, tA, tAS,
                     tAC, tB, tBS, p);
 }
 
