@@ -109,8 +109,9 @@ struct Cfg {
   static constexpr int kNumBars = 2 * STAGES + 2 * TSTAGES + 2 * SSTAGES + 2 * ABUF + 2 * NP + 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffSched = kOffMisc + 64;
-  // schedule: [E+1] chunk prefix, [E+1] row starts, [cap] int16 expert of each chunk (cap may be 0)
-  static int smem_bytes(int E, int cap) { return kOffSched + 2 * (E + 1) * 4 + 2 * cap + 16 + 1024; }
+  // schedule: [E+1] chunk prefix, [E+1] row starts, then (16-byte aligned) [cap] int4 tiles of this CTA
+  __host__ __device__ static int tiles_off(int E) { return (kOffSched + 2 * (E + 1) * 4 + 15) & ~15; }
+  static int smem_bytes(int E, int cap) { return tiles_off(E) + 16 * cap + 1024; }
   // tensor memory: [NP][GPS][NMAX] partials | [ABUF][GPS][32] converted weights (A_TMEM) |
   // with two epilogue sets, two NMAX-column slots (by tile parity) through which set 1 hands
   // its accumulators to set 0 at the end of a tile
@@ -160,7 +161,7 @@ struct GemmParams {
   int E, N, K, M;      // M: rows of A (dense) / M_total
   int gps;             // 128-K groups per stage (divides K/128, <= Cfg::GPS)
   int splits;          // K splits per tile (1: none)
-  int chunk_cap;       // entries of the chunk -> expert table in shared memory (0: binary search)
+  int tile_cap;        // tiles per CTA the shared-memory tile list holds (0: decode each tile in place)
 };
 
 // UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(256) prepack_kernel(const uint32_t* __restrict
 struct Sched {
   const int* prefix;  // [E+1] chunk prefix
   const int* start;   // [E+1] row starts
-  const int16_t* chunk_e;  // [chunks] expert of each chunk, or nullptr (binary search over prefix)
+  const int4* tiles;  // this CTA's tiles {e, nb, row0, rows} in order, or nullptr (decode in place)
   int E, NMAX, nblk;
   int S, Gs, gps;     // K splits per tile, stages per tile, groups per stage
   // item = tile * S + split; split s covers stages [s*Gs/S, (s+1)*Gs/S) of the tile
@@ -227,22 +228,30 @@ struct Sched {
     const int item = item_ / S;
     const int chunk = item / nblk;
     nb = item - chunk * nblk;
-    if (chunk_e) {
-      e = chunk_e[chunk];
-    } else {
-      int lo = 0, hi = E;  // prefix[lo] <= chunk < prefix[hi]
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (prefix[mid] <= chunk) lo = mid; else hi = mid;
-      }
-      e = lo;
+    int lo = 0, hi = E;  // prefix[lo] <= chunk < prefix[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prefix[mid] <= chunk) lo = mid; else hi = mid;
     }
+    e = lo;
     // chunks sit on a grid of NMAX rows from the expert's first row rounded down to 4, so a
     // tile's token rows start 4-aligned (16-byte scale vectors) and only the first one is ragged
     const int st = start[e], end = start[e + 1];
     const int base = (st & ~3) + (chunk - prefix[e]) * NMAX;
     row0 = max(st, base);
     rows = min(end, base + NMAX) - row0;
+  }
+  // tile `it` of this CTA (item = blockIdx.x + it * gridDim.x)
+  __device__ __forceinline__ void tile(int it, int item, int& e, int& nb, int& row0, int& rows) const {
+    if (tiles) {
+      const int4 t = tiles[it];
+      e = t.x;
+      nb = t.y;
+      row0 = t.z;
+      rows = t.w;
+    } else {
+      decode(item, e, nb, row0, rows);
+    }
   }
 };
 
@@ -341,7 +350,7 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
   const int E = prm.seg ? prm.E : 1;
   int* s_prefix = reinterpret_cast<int*>(smem + CF::kOffSched);  // [E+1]
   int* s_start = s_prefix + (E + 1);                              // [E+1]
-  int16_t* s_chunk_e = reinterpret_cast<int16_t*>(s_start + (E + 1));  // [chunk_cap]
+  int4* s_tiles = reinterpret_cast<int4*>(smem + CF::tiles_off(E));  // [tile_cap]
 
   pdl_trigger();  // the next kernel may launch once every CTA has started (it waits for this grid)
   const int warp = threadIdx.x >> 5;
@@ -423,20 +432,27 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
   __syncthreads();
   tc_fence_after();
 
-  // chunk -> expert table: every role decodes each of its tiles, and a binary search over the
-  // experts is a chain of dependent shared-memory loads (~1500 cycles per tile under load)
-  const int n_chunks = s_prefix[E];
-  const bool table = n_chunks <= prm.chunk_cap;
-  if (table) {
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-      for (int c = s_prefix[e]; c < s_prefix[e + 1]; ++c) s_chunk_e[c] = static_cast<int16_t>(e);
+  // This CTA's tiles, decoded once here by all threads (a tile's decode is a binary search over the
+  // experts, a chain of dependent shared-memory loads that cost each role ~1500 cycles per tile
+  // under load); every role then reads a tile with one 16-byte load.
+  const int S = SPLIT ? prm.splits : 1;  // 1 folds the split arithmetic away
+  Sched sch{s_prefix, s_start, nullptr, E, NMAX, nblk, S, G / gps, gps};
+  const int n_items = s_prefix[E] * nblk * S;
+  const int n_mine = n_items > static_cast<int>(blockIdx.x)
+                         ? (n_items - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                               static_cast<int>(gridDim.x)
+                         : 0;
+  if (n_mine <= prm.tile_cap) {
+    for (int i = threadIdx.x; i < n_mine; i += blockDim.x) {
+      int e, nb, row0, rows;
+      sch.decode(static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x), e, nb, row0, rows);
+      s_tiles[i] = make_int4(e, nb, row0, rows);
+    }
+    sch.tiles = s_tiles;
   }
   __syncthreads();
 
   const uint32_t tmem_base = *s_tmem;
-  const int S = SPLIT ? prm.splits : 1;  // 1 folds the split arithmetic away
-  Sched sch{s_prefix, s_start, table ? s_chunk_e : nullptr, E, NMAX, nblk, S, G / gps, gps};
-  const int n_items = n_chunks * nblk * S;
 
   // Counters: `it` counts 128-K groups, `st` counts stages of gps groups; stage st holds
   // groups [st*gps, st*gps + gps) of one tile (gps divides K/128, so stages never straddle
@@ -451,9 +467,9 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
         const uint64_t pol_w = l2_policy_evict_first();
         const uint32_t w_bytes = gps * CF::kWpkBytes;
         uint32_t st = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        for (int item = blockIdx.x, it = 0; item < n_items; item += gridDim.x, ++it) {
           int e, nb, row0, rows;
-          sch.decode(item, e, nb, row0, rows);
+          sch.tile(it, item, e, nb, row0, rows);
           int g_beg, g_end;
           sch.krange(item, g_beg, g_end);
           for (int g0 = g_beg; g0 < g_end; g0 += gps, ++st) {
@@ -471,9 +487,9 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
         const uint32_t t_bytes = gps * CF::kTokBytes;
         const uint32_t sc_bytes = gps * (2 * NMAX * 4 + kBM * 4);
         uint32_t st = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        for (int item = blockIdx.x, it = 0; item < n_items; item += gridDim.x, ++it) {
           int e, nb, row0, rows;
-          sch.decode(item, e, nb, row0, rows);
+          sch.tile(it, item, e, nb, row0, rows);
           const int r4 = row0 & ~3;
           int g_beg, g_end;
           sch.krange(item, g_beg, g_end);
@@ -500,9 +516,9 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
       const int mset = warp - kWarpMma;
       if (lane == 0) {
         uint32_t st = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        for (int item = blockIdx.x, it = 0; item < n_items; item += gridDim.x, ++it) {
           int e, nb, row0, rows;
-          sch.decode(item, e, nb, row0, rows);
+          sch.tile(it, item, e, nb, row0, rows);
           const int ncol = (row0 - (row0 & ~3) + rows + 15) & ~15;
           const uint32_t idesc = idesc_e4m3(static_cast<uint32_t>(ncol));
           int g_beg, g_end;
@@ -556,7 +572,7 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
     const int cset = (warp - kWarpConv0) / kConvWarps;
     const int r = q4 * 32 + lane;
     uint32_t st = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    for (int item = blockIdx.x, it = 0; item < n_items; item += gridDim.x, ++it) {
       int g_beg, g_end;
       sch.krange(item, g_beg, g_end);
       for (int g0 = g_beg; g0 < g_end; g0 += gps, ++st) {
@@ -640,9 +656,9 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
       const int cq = 2 * (lane & 3);
       const uint32_t t_lane = static_cast<uint32_t>(q4 * 32) << 16;
       uint32_t st = 0;
-      for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      for (int item = blockIdx.x, it = 0; item < n_items; item += gridDim.x, ++it) {
         int e, nb, row0, rows;
-        sch.decode(item, e, nb, row0, rows);
+        sch.tile(it, item, e, nb, row0, rows);
         const int r4 = row0 & ~3;
         const int lo = row0 - r4;    // columns [lo, lo + rows) of the tile are this chunk's rows
         const int need = lo + rows;  // 64-column blocks from `need` on are never stored: skipped
@@ -743,9 +759,9 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
       const uint32_t t_lane = static_cast<uint32_t>(q4 * 32) << 16;
       constexpr int CH = NHALF < 16 ? 8 : 16;  // columns per tensor-memory load
       uint32_t st = 0, tile = 0;
-      for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++tile) {
+      for (int item = blockIdx.x, it = 0; item < n_items; item += gridDim.x, ++tile, ++it) {
         int e, nb, row0, rows;
-        sch.decode(item, e, nb, row0, rows);
+        sch.tile(it, item, e, nb, row0, rows);
         const int r4 = row0 & ~3;
         const int lo = row0 - r4;   // columns [lo, lo + rows) of the tile are this chunk's rows
         const int need = lo + rows;  // columns past `need` are never stored: skip their promotion
@@ -1034,14 +1050,15 @@ int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, c
   p.gps = gps;
   p.partial = partial;
   p.splits = splits;
-  // chunk -> expert table: an expert's chunks sit on the NMAX grid from its first row rounded down to
-  // 4, so it has at most (3 + rows) / NMAX + 1 of them
+  // tile list: an expert's chunks sit on the NMAX grid from its first row rounded down to 4, so it
+  // has at most (3 + rows) / NMAX + 1 of them; tiles = chunks x 128-row blocks x K splits
   const int Ed = seg ? static_cast<int>(E) : 1;
-  const int64_t bound = seg ? (3 * E + M) / CF::NMAX + E + 1 : (M + CF::NMAX - 1) / CF::NMAX + 1;
-  const int64_t room = (kMaxDynSmem - CF::smem_bytes(Ed, 0)) / 2;
-  p.chunk_cap = static_cast<int>(std::max<int64_t>(0, std::min(bound, room)));
+  const int64_t chunks = seg ? (3 * E + M) / CF::NMAX + E + 1 : (M + CF::NMAX - 1) / CF::NMAX + 1;
+  const int64_t per_cta = ceil_div(chunks * (N / kBM) * std::max(splits, 1), num_sms());
+  const int64_t room = (kMaxDynSmem - CF::smem_bytes(Ed, 0)) / 16;
+  p.tile_cap = static_cast<int>(std::max<int64_t>(0, std::min(per_cta, room)));
   return launch_pdl("w4a8_gemm_kernel", splits > 1 ? w4a8_gemm_kernel<CF, true> : w4a8_gemm_kernel<CF, false>,
-                    dim3(num_sms()), dim3(CF::kThreads), CF::smem_bytes(Ed, p.chunk_cap), st, tA, tAS,
+                    dim3(num_sms()), dim3(CF::kThreads), CF::smem_bytes(Ed, p.tile_cap), st, tA, tAS,
                     tAC, tB, tBS, p);
 }
 
