@@ -76,6 +76,8 @@ def test_every_int4_value(lib, M):
     ([40, 200, 0, 129, 5, 300, 1, 77], 384, 512),    # several token chunks per expert
     ([1] * 37, 128, 1024),
     ([0, 0, 0, 500], 128, 128),
+    ([2, 0, 5, 1, 31, 3], 256, 4096),                # long K: the small-M pipeline with 4 MMA warps
+    ([7, 1, 0, 16, 9], 128, 7168),
 ])
 def test_grouped_gemm(lib, counts, N, K):
     rng = np.random.default_rng(sum(counts) + N + K)

@@ -1064,6 +1064,11 @@ int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, c
 
 // decode: few rows per expert, weight streaming; converted weights in tensor memory
 using CfgDecode = Cfg<16, 4, 5, 4, 6, 2, 3, true, 2, 2, 4, 1>;
+// the same with 4 MMA-issuing warps, for long K (many stages per tile): a thread stalls ~130 cycles per
+// tcgen05.mma, so 2 warps issuing 8 MMAs each per stage sit near the stage period; with short K the
+// extra warps cost more at the frequent tile changes than they save (grouped w13 / w2 of the decode
+// layer: 0.638 -> 0.624 ms / 0.335 -> 0.342 ms)
+using CfgDecodeLongK = Cfg<16, 4, 5, 4, 6, 2, 3, true, 2, 4, 4, 1>;
 // prefill: 128-row token tiles, one group per stage; converted weights in tensor memory
 using CfgPrefill = Cfg<128, 1, 8, 6, 8, 4, 2, true, 1, 2, 8, 1>;
 
@@ -1121,7 +1126,9 @@ int gemm_common(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_
   }
   int rc;
   // Few rows per expert: weight streaming, 16-wide token tiles and a deep ring.
-  if (M <= 32 * E)
+  if (M <= 32 * E && seg && K >= 4096)
+    rc = launch<CfgDecodeLongK>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st);
+  else if (M <= 32 * E)
     rc = launch<CfgDecode>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st);
   else
     rc = launch<CfgPrefill>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st);
