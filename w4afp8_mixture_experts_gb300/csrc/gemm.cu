@@ -1069,8 +1069,11 @@ using CfgDecode = Cfg<16, 4, 5, 4, 6, 2, 3, true, 2, 2, 4, 1>;
 // extra warps cost more at the frequent tile changes than they save (grouped w13 / w2 of the decode
 // layer: 0.638 -> 0.624 ms / 0.335 -> 0.342 ms)
 using CfgDecodeLongK = Cfg<16, 4, 5, 4, 6, 2, 3, true, 2, 4, 4, 1>;
-// prefill: 128-row token tiles, one group per stage; converted weights in tensor memory
-using CfgPrefill = Cfg<128, 1, 8, 6, 8, 4, 2, true, 1, 2, 8, 1>;
+// prefill: 128-row token tiles, two groups per stage (the stage's fixed costs of waits and hand-overs
+// paid once per two groups), so the fp32 partials of 2 slots x 2 groups fill the tensor memory and the
+// converted weights go to shared memory (prefill w13 4.378 -> 4.320 ms, w2 2.589 -> 2.504 ms against
+// one group per stage with the weights in tensor memory)
+using CfgPrefill = Cfg<128, 2, 4, 2, 4, 2, 2, false, 1, 2, 8, 1>;
 
 // C[m][n] = bf16(sum over s of partial[s][m][n]), four columns per thread.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ partial,
