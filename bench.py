@@ -261,8 +261,8 @@ class MoeRunner:
                 ("permute", lambda: lib.moe_permute_ep(p["topk_ids"], T, k, E, emap, EL, p["seg_indptr"],
                                                        p["src2dst"], p["dst2src"], p["permute_ws"],
                                                        self.permute_ws_bytes, stream)),
-                ("quant", lambda: lib.fp8_quant_per_token_group(x, T, H, p["dst2src"], k, P, p["xq"], p["xs"],
-                                                                p["xc"], ld, stream)),
+                ("quant", lambda: lib.fp8_quant_scatter_per_token_group(x, T, H, p["src2dst"], k, P, p["xq"],
+                                                                        p["xs"], p["xc"], ld, stream)),
                 ("w13", lambda: lib.w4a8_grouped_gemm(p["xq"], p["xs"], p["xc"], ld, w13, w13s, p["seg_indptr"], EL,
                                                       2 * I, H, P, p["y13"], None, 0, stream)),
                 ("silu_requant", lambda: lib.silu_mul_requant_rows(p["y13"], P, m_dev, I, p["hq"], p["hs"], p["hc"],
@@ -276,8 +276,8 @@ class MoeRunner:
             ("route", lambda: lib.moe_route_topk(lg, T, E, k, 1, p["topk_ids"], p["topk_w"], stream)),
             ("permute", lambda: lib.moe_permute(p["topk_ids"], T, k, E, p["seg_indptr"], p["src2dst"],
                                                 p["dst2src"], p["permute_ws"], self.permute_ws_bytes, stream)),
-            ("quant", lambda: lib.fp8_quant_per_token_group(x, T, H, p["dst2src"], k, P, p["xq"], p["xs"], p["xc"],
-                                                            ld, stream)),
+            ("quant", lambda: lib.fp8_quant_scatter_per_token_group(x, T, H, p["src2dst"], k, P, p["xq"], p["xs"],
+                                                                    p["xc"], ld, stream)),
             ("w13", lambda: lib.w4a8_grouped_gemm(p["xq"], p["xs"], p["xc"], ld, w13, w13s, p["seg_indptr"], E,
                                                   2 * I, H, P, p["y13"], None, 0, stream)),
             ("silu_requant", lambda: lib.silu_mul_requant(p["y13"], P, I, p["hq"], p["hs"], p["hc"], ld, stream)),

@@ -149,6 +149,20 @@ int fp8_quant_per_token_group(const uint16_t* x, int64_t M_src, int64_t K,
                               uint8_t* q, float* scales, float* gcorr, int64_t scale_ld, void* stream);
 
 /*
+ * (3') The same quantisation of the permuted copy, scattered from the source
+ * rows: each row t of x [T][K] is quantised once and its codes, scales and
+ * gcorr are written to rows src2dst[t*k + j] of q (j < k); entries of -1 (a
+ * pair of another expert-parallel shard) or >= M_out are skipped.  With
+ * src2dst from (2) this writes exactly what (3) with row_index = dst2src,
+ * row_div = k writes, computing each token's row once instead of k times.
+ *   x bf16 [T][K]   src2dst int32 [T*k]   q uint8 [M_out][K]
+ *   scales, gcorr fp32 [K/128][scale_ld]   1 <= k <= 32, other rules as (3).
+ */
+int fp8_quant_scatter_per_token_group(const uint16_t* x, int64_t T, int64_t K, const int32_t* src2dst, int k,
+                                      int64_t M_out, uint8_t* q, float* scales, float* gcorr, int64_t scale_ld,
+                                      void* stream);
+
+/*
  * (4) Grouped int4 x FP8 GEMM (PR #7762 page: CUTLASS W4A8 grouped GEMM,
  * chunk_size 128).  For expert e and rows j in [seg_indptr[e], seg_indptr[e+1]):
  *   C[j][n] = bf16( sum_g a_s[g][j] * b_s[e][g][n] *
@@ -231,8 +245,8 @@ int w4a8_linear(const uint8_t* A, const float* a_scales, const float* a_gcorr, i
 size_t w4a8_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int64_t E);
 
 /*
- * The whole layer in one call: (1) route -> (2) permute -> (3) quantise the
- * permuted hidden states -> (4) w13 -> (5) SiLU and Mul + requantise -> (4) w2
+ * The whole layer in one call: (1) route -> (2) permute -> (3') quantise the
+ * hidden states into their permuted places -> (4) w13 -> (5) SiLU and Mul + requantise -> (4) w2
  * -> (6) combine.  Seven launches (plus the permutation's), nothing else.
  *   x bf16 [T][H]   logits fp32 [T][E]
  *   w13 uint8 [E][2I][H/2] prepacked (rows [0, I) gate, [I, 2I) up)   w13_s fp32 [E][H/128][2I]

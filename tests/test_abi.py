@@ -30,7 +30,8 @@ def test_every_declared_symbol_is_exported(clib):
     assert len(names) >= 16
     for n in ["moe_route_topk", "moe_permute", "fp8_quant_per_token_group", "w4a8_grouped_gemm",
               "silu_mul_requant", "moe_unpermute_combine", "w4a8_linear", "w4a8_prepack_weights",
-              "w4a8_moe_forward", "w4a8_moe_forward_noalloc", "moe_permute_ep", "w4a8_moe_forward_ep"]:
+              "w4a8_moe_forward", "w4a8_moe_forward_noalloc", "moe_permute_ep", "w4a8_moe_forward_ep",
+              "fp8_quant_scatter_per_token_group", "silu_mul_requant_rows"]:
         assert n in names
     for n in names:
         assert hasattr(clib, n), n
@@ -57,6 +58,8 @@ P16 = ctypes.c_void_p(16)  # a 16-byte aligned non-null dummy (never dereference
     (lambda L: L.moe_permute_ep(P16, 1024, 8, 256, P16, 32, P16, P16, P16, NULL, 0, NULL), b"workspace"),
     (lambda L: L.fp8_quant_per_token_group(P16, 4, 100, NULL, 1, 4, P16, P16, NULL, 4, NULL), b"K=100"),
     (lambda L: L.fp8_quant_per_token_group(P16, 4, 128, NULL, 1, 4, P16, P16, NULL, 2, NULL), b"scale_ld"),
+    (lambda L: L.fp8_quant_scatter_per_token_group(P16, 4, 100, P16, 2, 8, P16, P16, NULL, 8, NULL), b"K=100"),
+    (lambda L: L.fp8_quant_scatter_per_token_group(P16, 4, 128, P16, 33, 8, P16, P16, NULL, 8, NULL), b"k=33"),
     (lambda L: L.w4a8_grouped_gemm(P16, P16, P16, 4, P16, P16, P16, 2, 256, 200, 4, P16, NULL, 0, NULL), b"K=200"),
     (lambda L: L.w4a8_grouped_gemm(P16, P16, P16, 4, P16, P16, P16, 2, 100, 256, 4, P16, NULL, 0, NULL), b"N=100"),
     (lambda L: L.w4a8_grouped_gemm(P16, P16, P16, 4, P16, P16, NULL, 2, 128, 256, 4, P16, NULL, 0, NULL),

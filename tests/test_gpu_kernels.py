@@ -176,3 +176,30 @@ def test_prepack_weights(lib, rows, K):
     packed[0, :4] = [0x00, 0x88, 0x7F, 0xF8]
     got = lib.w4a8_prepack_weights(to_dev(packed)).cpu().numpy()
     assert np.array_equal(decode_prepacked(got), oracle.unpack_int4(packed))
+
+
+@pytest.mark.parametrize("T,K,k,drop", [(1, 128, 1, 0.0), (64, 7168, 8, 0.0), (300, 512, 3, 0.0),
+                                        (1000, 256, 8, 0.5), (5000, 1024, 4, 0.0)])
+def test_quant_scatter_equals_gather(lib, T, K, k, drop):
+    # quantising each source row once and scattering it through src2dst writes exactly what the gather
+    # through dst2src writes (codes, scales, corrections), and matches the oracle on the placed rows
+    rng = np.random.default_rng(T + K + k)
+    x_bits = inputs.to_bf16_bits(rng.standard_normal((T, K)).astype(np.float32))
+    P = T * k
+    s2d = rng.permutation(P).astype(np.int32)
+    s2d[rng.random(P) < drop] = -1  # pairs of another expert-parallel shard
+    PL = int((s2d >= 0).sum())
+    keep = np.nonzero(s2d >= 0)[0]
+    s2d[keep] = np.argsort(np.argsort(s2d[keep])).astype(np.int32)  # placed rows are 0 .. PL-1
+    d2s = np.full(P, -1, np.int32)
+    d2s[s2d[keep]] = keep.astype(np.int32)
+    x = bf16_from_bits(x_bits)
+    sq, ss, sc = lib.fp8_quant_scatter_per_token_group(x, to_dev(s2d), k, P)
+    gq, gs, gc = lib.fp8_quant_per_token_group(x, to_dev(d2s), k)
+    torch.cuda.synchronize()
+    assert torch.equal(sq[:PL], gq[:PL]) and torch.equal(ss[:, :PL], gs[:, :PL]) and torch.equal(sc[:, :PL], gc[:, :PL])
+    rq, rsc = oracle.quant_per_token_group(inputs.bf16_bits_to_f32(x_bits))
+    src = d2s[:PL] // k
+    assert np.array_equal(sq[:PL].cpu().numpy(), rq[src])
+    assert np.array_equal(ss[:, :PL].cpu().numpy().T, rsc[src])
+    assert bool((sq[PL:] == 0).all())

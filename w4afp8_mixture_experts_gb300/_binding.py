@@ -30,6 +30,8 @@ _SIGS = {
                                 _c_vp]),
     "fp8_quant_per_token_group": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp,
                                            _c_i64, _c_vp]),
+    "fp8_quant_scatter_per_token_group": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_vp, _c_vp,
+                                                   _c_vp, _c_i64, _c_vp]),
     "w4a8_grouped_gemm": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64,
                                    _c_i64, _c_vp, _c_vp, _c_sz, _c_vp]),
     "w4a8_prepack_weights": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_vp]),
@@ -154,6 +156,21 @@ def moe_permute_ep(topk_ids, E: int, expert_map, E_local: int):
     _check(load().moe_permute_ep(_p(topk_ids), T, k, E, _p(expert_map), E_local, _p(seg), _p(s2d), _p(d2s), _p(ws),
                                  need, _stream()))
     return seg, s2d, d2s
+
+
+def fp8_quant_scatter_per_token_group(x, src2dst, k: int, m_out: int):
+    """bf16 [T, K] -> codes uint8 [m_out, K], scales and gcorr fp32 [K/128, ld]: row t quantised once and
+    written to rows src2dst[t*k + j] (-1 skipped; rows nothing maps to are left zero here)."""
+    _req(x, torch.bfloat16, "x", 2)
+    _req(src2dst, torch.int32, "src2dst", 1)
+    T, K = x.shape
+    ld = scale_ld(m_out)
+    q = torch.zeros((m_out, K), dtype=torch.uint8, device=x.device)
+    s = torch.zeros((max(1, K // 128), ld), dtype=torch.float32, device=x.device)
+    c = torch.zeros((max(1, K // 128), ld), dtype=torch.float32, device=x.device)
+    _check(load().fp8_quant_scatter_per_token_group(_p(x), T, K, _p(src2dst), k, m_out, _p(q), _p(s), _p(c), ld,
+                                                    _stream()))
+    return q, s, c
 
 
 def fp8_quant_per_token_group(x, row_index=None, row_div: int = 1, m_out: int | None = None):

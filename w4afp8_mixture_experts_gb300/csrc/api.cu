@@ -153,7 +153,7 @@ extern "C" int w4a8_moe_forward(const uint16_t* x, const float* logits, int64_t 
   const int64_t P = T * k;
   if ((rc = moe_route_topk(logits, T, E, k, renormalize, ids, tw, stream))) return rc;
   if ((rc = moe_permute(ids, T, k, E, seg, s2d, d2s, b + L.permute_ws, permute_ws_bytes(P, E), stream))) return rc;
-  if ((rc = fp8_quant_per_token_group(x, T, H, d2s, k, P, xq, xs, xc, L.scale_ld, stream))) return rc;
+  if ((rc = fp8_quant_scatter_per_token_group(x, T, H, s2d, k, P, xq, xs, xc, L.scale_ld, stream))) return rc;
   if ((rc = w4a8_grouped_gemm(xq, xs, xc, L.scale_ld, w13, w13_s, seg, E, 2 * I, H, P, y13, nullptr, 0, stream)))
     return rc;
   if ((rc = silu_mul_requant(y13, P, I, hq, hs, hc, L.scale_ld, stream))) return rc;
@@ -195,7 +195,7 @@ extern "C" int w4a8_moe_forward_ep(const uint16_t* x, const float* logits, int64
   if ((rc = moe_permute_ep(ids, T, k, E, expert_map, E_local, seg, s2d, d2s, b + L.permute_ws,
                            permute_ws_bytes(P, E_local), stream)))
     return rc;
-  if ((rc = fp8_quant_per_token_group(x, T, H, d2s, k, P, xq, xs, xc, L.scale_ld, stream))) return rc;
+  if ((rc = fp8_quant_scatter_per_token_group(x, T, H, s2d, k, P, xq, xs, xc, L.scale_ld, stream))) return rc;
   if ((rc = w4a8_grouped_gemm(xq, xs, xc, L.scale_ld, w13, w13_s, seg, E_local, 2 * I, H, P, y13, nullptr, 0,
                               stream)))
     return rc;

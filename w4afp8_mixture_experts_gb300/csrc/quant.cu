@@ -115,6 +115,84 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// The same quantisation, once per source row t, with the codes, scale and correction written to
+// every destination row src2dst[t*k + j] (j < k; -1 and rows past M_out are skipped): in the MoE
+// each token's row is quantised once instead of once per routed pair.
+template <int LANES>
+__global__ void __launch_bounds__(256)
+    quant_scatter_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t K, const int32_t* __restrict__ src2dst,
+                         int k, int64_t M_out, uint8_t* __restrict__ q, float* __restrict__ scales,
+                         float* __restrict__ gcorr, int64_t ld) {
+  constexpr int kQuantVals = kGroup / LANES;  // values per lane
+  pdl_trigger();
+  pdl_wait();
+  const int64_t G = K / kGroup;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t task = tid / LANES;
+  const int sub = static_cast<int>(tid % LANES);
+  if (task >= T * G) return;  // a group's lanes leave together
+  const int64_t row = task / G;
+  const int64_t g = task - row * G;
+  const uint4* xp = reinterpret_cast<const uint4*>(x + row * K + g * kGroup + sub * kQuantVals);
+  uint32_t w[kQuantVals / 2];
+  uint32_t mx = 0;
+#pragma unroll
+  for (int i = 0; i < kQuantVals / 8; ++i) {
+    const uint4 v = __ldg(xp + i);
+    w[4 * i + 0] = v.x;
+    w[4 * i + 1] = v.y;
+    w[4 * i + 2] = v.z;
+    w[4 * i + 3] = v.w;
+    mx = __vmaxu2(mx, __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu));
+    mx = __vmaxu2(mx, __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+  }
+  mx = max(mx & 0xFFFFu, mx >> 16);
+  const unsigned quad = ((1u << LANES) - 1u) << (threadIdx.x & (32 - LANES));  // this group's lanes
+#pragma unroll
+  for (int o = 1; o < LANES; o <<= 1) mx = max(mx, __shfl_xor_sync(quad, mx, o));
+  const float amax = fmaxf(__uint_as_float(mx << 16), 1e-12f);
+  const float s = __fdiv_rn(amax, 448.0f);
+  const float r = __frcp_rn(s);
+  uint32_t code[kQuantVals / 4];  // 4 codes per word
+  float sum = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kQuantVals / 8; ++i) {
+    uint32_t c[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t v = w[4 * i + j];
+      c[j] = e4m3x2(div_by_scale(bf16_lo(v), s, r), div_by_scale(bf16_hi(v), s, r));
+    }
+    if (gcorr) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t h2;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(c[j])));
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+        sum += f.x + f.y;
+      }
+    }
+    code[2 * i] = c[0] | (c[1] << 16);
+    code[2 * i + 1] = c[2] | (c[3] << 16);
+  }
+  if (gcorr) {
+#pragma unroll
+    for (int o = 1; o < LANES; o <<= 1) sum += __shfl_xor_sync(quad, sum, o);
+  }
+  const float corr = -0.5f * __fmul_rn(s, sum);
+  for (int j = 0; j < k; ++j) {
+    const int64_t d = src2dst[row * k + j];  // the same for all of the group's lanes
+    if (d < 0 || d >= M_out) continue;
+    uint2* qp = reinterpret_cast<uint2*>(q + d * K + g * kGroup + sub * kQuantVals);
+#pragma unroll
+    for (int i = 0; i < kQuantVals / 8; ++i) qp[i] = make_uint2(code[2 * i], code[2 * i + 1]);
+    if (sub == 0) {
+      scales[g * ld + d] = s;
+      if (gcorr) gcorr[g * ld + d] = corr;
+    }
+  }
+}
+
 // h = silu(gate) * up = gate / (1 + exp(-gate)) * up, fp32.
 __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
@@ -213,6 +291,28 @@ extern "C" int fp8_quant_per_token_group(const uint16_t* x, int64_t M_src, int64
   return launch_pdl("quant_quad_kernel", small ? quant_quad_kernel<16> : quant_quad_kernel<4>,
                     dim3(static_cast<unsigned>(blocks)), dim3(256), 0, static_cast<cudaStream_t>(stream), x, K,
                     row_index, row_div, M_out, q, scales, gcorr, scale_ld);
+}
+
+extern "C" int fp8_quant_scatter_per_token_group(const uint16_t* x, int64_t T, int64_t K, const int32_t* src2dst,
+                                                 int k, int64_t M_out, uint8_t* q, float* scales, float* gcorr,
+                                                 int64_t scale_ld, void* stream) {
+  using namespace w4a8;
+  W4A8_REQUIRE(K > 0 && K % kGroup == 0, "K=%lld must be a positive multiple of 128", (long long)K);
+  W4A8_REQUIRE(T >= 0 && M_out >= 0, "negative row count");
+  W4A8_REQUIRE(k >= 1 && k <= 32, "k=%d must be in [1, 32]", k);
+  W4A8_REQUIRE(scale_ld >= M_out && scale_ld % 4 == 0, "scale_ld must be >= M_out and a multiple of 4");
+  if (T == 0 || M_out == 0) return W4A8_OK;
+  W4A8_REQUIRE(x && src2dst && q && scales, "null pointer");
+  W4A8_REQUIRE(((uintptr_t)x & 15) == 0 && ((uintptr_t)q & 7) == 0 && ((uintptr_t)scales & 3) == 0 &&
+                   ((uintptr_t)gcorr & 3) == 0,
+               "x must be 16-byte, q 8-byte and scales, gcorr 4-byte aligned");
+  const int64_t groups = T * (K / kGroup);
+  const bool small = groups < kSmallLaunchGroups;
+  const int64_t blocks = ceil_div(groups * (small ? 16 : 4), 256);
+  W4A8_REQUIRE(blocks < (1ll << 31), "too many rows");
+  return launch_pdl("quant_scatter_kernel", small ? quant_scatter_kernel<16> : quant_scatter_kernel<4>,
+                    dim3(static_cast<unsigned>(blocks)), dim3(256), 0, static_cast<cudaStream_t>(stream), x, T, K,
+                    src2dst, k, M_out, q, scales, gcorr, scale_ld);
 }
 
 extern "C" int silu_mul_requant_rows(const uint16_t* gate_up, int64_t M, const int64_t* m_dev, int64_t I,
