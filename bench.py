@@ -427,8 +427,9 @@ def run_ours(args, name, cfg):
         "stages_note": "stage breakdown from a separate pass with an event after every stage; the timed "
                        "region runs the stages back to back with events only around w13",
         "roofline": roof,
-        # the permutation is two kernels (count + placement) from 8192 routed pairs
-        "gpu_launches": (nst + (1 if r.permute_ws_bytes else 0)) * K,
+        # the permutation is two kernels (count + placement) from 8192 routed pairs; with 32 to 128 rows per
+        # expert on average each grouped GEMM is two kernels (experts up to 16 rows, then the rest)
+        "gpu_launches": (nst + (1 if r.permute_ws_bytes else 0) + (2 if 32 * r.EL < T * k < 128 * r.EL else 0)) * K,
         "clocks": clk.summary(),
     }
     if not args.no_e2e:

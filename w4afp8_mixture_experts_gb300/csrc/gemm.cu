@@ -59,7 +59,8 @@ constexpr int kWarpTmaAct = 1;               // producer of the token and scale 
 constexpr int kWarpMma = 2;                  // warps 2 .. 1 + kMmaWarps issue the MMAs
 constexpr int kConvWarps = 4;                // converter warps per set: one per tensor-memory lane quarter
 constexpr int kMaxExperts = 1024;
-constexpr int kMaxDynSmem = 227 * 1024;  // dynamic shared memory a CTA may use on sm_100 / sm_103
+constexpr int kMaxDynSmem = 227 * 1024;
+constexpr int kSmallExpertRows = 16;  // grouped GEMM with many rows: experts up to this many rows take 16-wide tiles  // dynamic shared memory a CTA may use on sm_100 / sm_103
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s: no legitimate wait comes close
 
 __device__ unsigned int g_gemm_error;
@@ -162,6 +163,7 @@ struct GemmParams {
   int gps;             // 128-K groups per stage (divides K/128, <= Cfg::GPS)
   int splits;          // K splits per tile (1: none)
   int tile_cap;        // tiles per CTA the shared-memory tile list holds (0: decode each tile in place)
+  int min_rows, max_rows;  // experts with a row count outside [min_rows, max_rows] are left to another launch
 };
 
 // UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -418,6 +420,7 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
         s_start[e] = st;
       }
       int v = cnt > 0 ? ((st & 3) + cnt + NMAX - 1) / NMAX : 0;  // chunks on the NMAX-row grid
+      if (cnt < prm.min_rows || cnt > prm.max_rows) v = 0;        // another launch's expert
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int u = __shfl_up_sync(0xffffffffu, v, o);
@@ -986,7 +989,7 @@ int plan_splits(int64_t M, int64_t N, int64_t K, int sms) {
 template <class CF>
 int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, const uint8_t* B, const float* b_s,
            const int64_t* seg, int64_t E, int64_t N, int64_t K, int64_t M, uint16_t* C, float* partial, int splits,
-           cudaStream_t st) {
+           cudaStream_t st, int min_rows = 1, int max_rows = 0x7fffffff) {
   const int64_t G = K / kGroup;
   const int gps = stage_groups<CF>(K);
   CUtensorMap tA, tAS, tAC, tB, tBS;
@@ -1050,6 +1053,8 @@ int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, c
   p.gps = gps;
   p.partial = partial;
   p.splits = splits;
+  p.min_rows = min_rows;
+  p.max_rows = max_rows;
   // tile list: an expert's chunks sit on the NMAX grid from its first row rounded down to 4, so it
   // has at most (3 + rows) / NMAX + 1 of them; tiles = chunks x 128-row blocks x K splits
   const int Ed = seg ? static_cast<int>(E) : 1;
@@ -1133,7 +1138,19 @@ int gemm_common(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_
     rc = launch<CfgDecodeLongK>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st);
   else if (M <= 32 * E)
     rc = launch<CfgDecode>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st);
-  else
+  else if (seg && M < 128 * E) {
+    // Fewer rows than one 128-wide tile per expert on average, so (skewed routing) many experts may hold
+    // only a few: experts with at most kSmallExpertRows rows take the 16-wide tiles, the rest the
+    // 128-wide ones, in two launches over disjoint experts.  A 128-wide tile converts and promotes as
+    // much for 5 rows as for 128 (skewed layer 4.13 -> 3.81 ms).  With more rows per expert the second
+    // launch would mostly find nothing to do and cost its start-up (~20 us).
+    rc = K >= 4096 ? launch<CfgDecodeLongK>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st, 1,
+                                            kSmallExpertRows)
+                   : launch<CfgDecode>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st, 1,
+                                       kSmallExpertRows);
+    if (rc == W4A8_OK)
+      rc = launch<CfgPrefill>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st, kSmallExpertRows + 1);
+  } else
     rc = launch<CfgPrefill>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st);
   if (rc != W4A8_OK || S == 1) return rc;
   const int64_t MN = M * N;  // N % 128 == 0, so MN % 4 == 0
