@@ -156,7 +156,8 @@ int fp8_quant_per_token_group(const uint16_t* x, int64_t M_src, int64_t K,
  * src2dst from (2) this writes exactly what (3) with row_index = dst2src,
  * row_div = k writes, computing each token's row once instead of k times.
  *   x bf16 [T][K]   src2dst int32 [T*k]   q uint8 [M_out][K]
- *   scales, gcorr fp32 [K/128][scale_ld]   1 <= k <= 32, other rules as (3).
+ *   scales, gcorr fp32 [K/128][scale_ld]   1 <= k <= 32; x and q 16-byte aligned,
+ *   scales and gcorr 4-byte aligned; other rules as (3).
  */
 int fp8_quant_scatter_per_token_group(const uint16_t* x, int64_t T, int64_t K, const int32_t* src2dst, int k,
                                       int64_t M_out, uint8_t* q, float* scales, float* gcorr, int64_t scale_ld,

@@ -180,15 +180,29 @@ __global__ void __launch_bounds__(256)
     for (int o = 1; o < LANES; o <<= 1) sum += __shfl_xor_sync(quad, sum, o);
   }
   const float corr = -0.5f * __fmul_rn(s, sum);
-  for (int j = 0; j < k; ++j) {
-    const int64_t d = src2dst[row * k + j];  // the same for all of the group's lanes
-    if (d < 0 || d >= M_out) continue;
-    uint2* qp = reinterpret_cast<uint2*>(q + d * K + g * kGroup + sub * kQuantVals);
+  constexpr int kPre = 8;  // destinations fetched ahead (top-8 routing: all of them)
+  for (int j0 = 0; j0 < k; j0 += kPre) {
+    int64_t dst[kPre];
 #pragma unroll
-    for (int i = 0; i < kQuantVals / 8; ++i) qp[i] = make_uint2(code[2 * i], code[2 * i + 1]);
-    if (sub == 0) {
-      scales[g * ld + d] = s;
-      if (gcorr) gcorr[g * ld + d] = corr;
+    for (int j = 0; j < kPre; ++j) dst[j] = j0 + j < k ? src2dst[row * k + j0 + j] : -1;
+#pragma unroll
+    for (int j = 0; j < kPre; ++j) {
+      const int64_t d = dst[j];  // the same for all of the group's lanes
+      if (d < 0 || d >= M_out) continue;
+      uint8_t* qp = q + d * K + g * kGroup + sub * kQuantVals;
+      if constexpr (kQuantVals % 16 == 0) {  // 16-byte stores (the lane's bytes are 16-byte aligned)
+#pragma unroll
+        for (int i = 0; i < kQuantVals / 16; ++i)
+          reinterpret_cast<uint4*>(qp)[i] = make_uint4(code[4 * i], code[4 * i + 1], code[4 * i + 2], code[4 * i + 3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kQuantVals / 8; ++i)
+          reinterpret_cast<uint2*>(qp)[i] = make_uint2(code[2 * i], code[2 * i + 1]);
+      }
+      if (sub == 0) {
+        scales[g * ld + d] = s;
+        if (gcorr) gcorr[g * ld + d] = corr;
+      }
     }
   }
 }
@@ -303,9 +317,9 @@ extern "C" int fp8_quant_scatter_per_token_group(const uint16_t* x, int64_t T, i
   W4A8_REQUIRE(scale_ld >= M_out && scale_ld % 4 == 0, "scale_ld must be >= M_out and a multiple of 4");
   if (T == 0 || M_out == 0) return W4A8_OK;
   W4A8_REQUIRE(x && src2dst && q && scales, "null pointer");
-  W4A8_REQUIRE(((uintptr_t)x & 15) == 0 && ((uintptr_t)q & 7) == 0 && ((uintptr_t)scales & 3) == 0 &&
+  W4A8_REQUIRE(((uintptr_t)x & 15) == 0 && ((uintptr_t)q & 15) == 0 && ((uintptr_t)scales & 3) == 0 &&
                    ((uintptr_t)gcorr & 3) == 0,
-               "x must be 16-byte, q 8-byte and scales, gcorr 4-byte aligned");
+               "x and q must be 16-byte, scales and gcorr 4-byte aligned");
   const int64_t groups = T * (K / kGroup);
   const bool small = groups < kSmallLaunchGroups;
   const int64_t blocks = ceil_div(groups * (small ? 16 : 4), 256);
