@@ -17,3 +17,12 @@ def test_tiny_layer_fixture():
     for key in ("out_sum", "out_abs_sum", "y13_abs_sum"):  # float sums: summation order may vary
         assert math.isclose(got.pop(key), want.pop(key), rel_tol=1e-12)
     assert got == want
+
+
+def test_tiny_shard_fixture():
+    with open(os.path.join(HERE, "golden", "oracle_tiny_shard.json")) as f:
+        want = json.load(f)
+    got = make_golden.compute_shard()
+    for key in ("out_sum", "out_abs_sum"):
+        assert math.isclose(got.pop(key), want.pop(key), rel_tol=1e-12)
+    assert got == want
