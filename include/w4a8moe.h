@@ -142,7 +142,7 @@ int moe_permute_ep(const int32_t* topk_ids, int64_t T, int k, int64_t E, const i
  * shard's dst2src) are skipped: q, scales and gcorr keep their old contents.
  *   x bf16 [M_src][K]   q uint8 [M_out][K]   scales, gcorr fp32 [K/128][scale_ld]
  *   K % 128 == 0, scale_ld >= M_out, scale_ld % 4 == 0.  gcorr may be NULL.
- *   x 16-byte aligned, q 8-byte aligned, scales and gcorr 4-byte aligned.
+ *   x and q 16-byte aligned, scales and gcorr 4-byte aligned.
  */
 int fp8_quant_per_token_group(const uint16_t* x, int64_t M_src, int64_t K,
                               const int32_t* row_index, int64_t row_div, int64_t M_out,

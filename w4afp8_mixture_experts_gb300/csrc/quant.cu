@@ -44,6 +44,77 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // Lanes per group: 4 for large launches, 16 for small ones (more threads in flight).
 constexpr int kSmallLaunchGroups = 1 << 16;
 
+// One (row, 128-group) quantised by its LANES lanes, lane `sub` holding values [sub*V, sub*V + V)
+// (V = 128 / LANES) of the group at xg: the codes (4 per word) stay in registers, with the scale s
+// and the group correction -1/2 * s * sum(E4M3 values) (when want_corr) returned to every lane.
+template <int LANES>
+__device__ __forceinline__ void quantize_group(const uint16_t* __restrict__ xg, int sub, bool want_corr,
+                                               uint32_t (&code)[kGroup / LANES / 4], float& s, float& corr) {
+  constexpr int kQuantVals = kGroup / LANES;  // values per lane
+  const uint4* xp = reinterpret_cast<const uint4*>(xg + sub * kQuantVals);
+  uint32_t w[kQuantVals / 2];
+  uint32_t mx = 0;
+#pragma unroll
+  for (int i = 0; i < kQuantVals / 8; ++i) {
+    const uint4 v = __ldg(xp + i);
+    w[4 * i + 0] = v.x;
+    w[4 * i + 1] = v.y;
+    w[4 * i + 2] = v.z;
+    w[4 * i + 3] = v.w;
+    mx = __vmaxu2(mx, __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu));
+    mx = __vmaxu2(mx, __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+  }
+  mx = max(mx & 0xFFFFu, mx >> 16);
+  const unsigned quad = ((1u << LANES) - 1u) << (threadIdx.x & (32 - LANES));  // this group's lanes
+#pragma unroll
+  for (int o = 1; o < LANES; o <<= 1) mx = max(mx, __shfl_xor_sync(quad, mx, o));
+  const float amax = fmaxf(__uint_as_float(mx << 16), 1e-12f);
+  s = __fdiv_rn(amax, 448.0f);
+  const float r = __frcp_rn(s);
+  float sum = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kQuantVals / 8; ++i) {
+    uint32_t c[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t v = w[4 * i + j];
+      c[j] = e4m3x2(div_by_scale(bf16_lo(v), s, r), div_by_scale(bf16_hi(v), s, r));
+    }
+    if (want_corr) {
+      // E4M3 pairs -> f16 pairs (exact) -> fp32 partial sums
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t h2;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(c[j])));
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+        sum += f.x + f.y;
+      }
+    }
+    code[2 * i] = c[0] | (c[1] << 16);
+    code[2 * i + 1] = c[2] | (c[3] << 16);
+  }
+  if (want_corr) {
+#pragma unroll
+    for (int o = 1; o < LANES; o <<= 1) sum += __shfl_xor_sync(quad, sum, o);
+  }
+  corr = -0.5f * __fmul_rn(s, sum);
+}
+
+// The lane's codes of one group to q (16-byte stores when a lane holds a multiple of 16 codes).
+template <int LANES>
+__device__ __forceinline__ void store_codes(uint8_t* qp, const uint32_t (&code)[kGroup / LANES / 4]) {
+  constexpr int kQuantVals = kGroup / LANES;
+  if constexpr (kQuantVals % 16 == 0) {
+#pragma unroll
+    for (int i = 0; i < kQuantVals / 16; ++i)
+      reinterpret_cast<uint4*>(qp)[i] = make_uint4(code[4 * i], code[4 * i + 1], code[4 * i + 2], code[4 * i + 3]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < kQuantVals / 8; ++i) reinterpret_cast<uint2*>(qp)[i] = make_uint2(code[2 * i], code[2 * i + 1]);
+  }
+}
+
+// Output row `row` of q from input row row_index[row] / row_div (or row itself): a gather.
 template <int LANES>
 __global__ void __launch_bounds__(256)
     quant_quad_kernel(const uint16_t* __restrict__ x, int64_t K, const int32_t* __restrict__ row_index,
@@ -63,55 +134,13 @@ __global__ void __launch_bounds__(256)
   const int64_t ri = row_index ? static_cast<int64_t>(row_index[row]) : row;
   if (ri < 0) return;  // no source row (a pair of a remote expert): left unwritten; the group's lanes leave together
   const int64_t src = row_index ? ri / row_div : row;
-  const uint4* xp = reinterpret_cast<const uint4*>(x + src * K + g * kGroup + sub * kQuantVals);
-  uint32_t w[kQuantVals / 2];
-  uint32_t mx = 0;
-#pragma unroll
-  for (int i = 0; i < kQuantVals / 8; ++i) {
-    const uint4 v = __ldg(xp + i);
-    w[4 * i + 0] = v.x;
-    w[4 * i + 1] = v.y;
-    w[4 * i + 2] = v.z;
-    w[4 * i + 3] = v.w;
-    mx = __vmaxu2(mx, __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu));
-    mx = __vmaxu2(mx, __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-  }
-  mx = max(mx & 0xFFFFu, mx >> 16);
-  const unsigned quad = ((1u << LANES) - 1u) << (threadIdx.x & (32 - LANES));  // this group's lanes
-#pragma unroll
-  for (int o = 1; o < LANES; o <<= 1) mx = max(mx, __shfl_xor_sync(quad, mx, o));
-  const float amax = fmaxf(__uint_as_float(mx << 16), 1e-12f);
-  const float s = __fdiv_rn(amax, 448.0f);
-  const float r = __frcp_rn(s);
-  uint8_t* qp = q + row * K + g * kGroup + sub * kQuantVals;
-  float sum = 0.0f;
-#pragma unroll
-  for (int i = 0; i < kQuantVals / 8; ++i) {
-    uint32_t c[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t v = w[4 * i + j];
-      c[j] = e4m3x2(div_by_scale(bf16_lo(v), s, r), div_by_scale(bf16_hi(v), s, r));
-    }
-    if (gcorr) {
-      // E4M3 pairs -> f16 pairs (exact) -> fp32 partial sums
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t h2;
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(c[j])));
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-        sum += f.x + f.y;
-      }
-    }
-    reinterpret_cast<uint2*>(qp)[i] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-  }
-  if (gcorr) {
-#pragma unroll
-    for (int o = 1; o < LANES; o <<= 1) sum += __shfl_xor_sync(quad, sum, o);
-  }
+  uint32_t code[kQuantVals / 4];
+  float s, corr;
+  quantize_group<LANES>(x + src * K + g * kGroup, sub, gcorr != nullptr, code, s, corr);
+  store_codes<LANES>(q + row * K + g * kGroup + sub * kQuantVals, code);
   if (sub == 0) {
     scales[g * ld + row] = s;
-    if (gcorr) gcorr[g * ld + row] = -0.5f * __fmul_rn(s, sum);
+    if (gcorr) gcorr[g * ld + row] = corr;
   }
 }
 
@@ -133,53 +162,9 @@ __global__ void __launch_bounds__(256)
   if (task >= T * G) return;  // a group's lanes leave together
   const int64_t row = task / G;
   const int64_t g = task - row * G;
-  const uint4* xp = reinterpret_cast<const uint4*>(x + row * K + g * kGroup + sub * kQuantVals);
-  uint32_t w[kQuantVals / 2];
-  uint32_t mx = 0;
-#pragma unroll
-  for (int i = 0; i < kQuantVals / 8; ++i) {
-    const uint4 v = __ldg(xp + i);
-    w[4 * i + 0] = v.x;
-    w[4 * i + 1] = v.y;
-    w[4 * i + 2] = v.z;
-    w[4 * i + 3] = v.w;
-    mx = __vmaxu2(mx, __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu));
-    mx = __vmaxu2(mx, __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-  }
-  mx = max(mx & 0xFFFFu, mx >> 16);
-  const unsigned quad = ((1u << LANES) - 1u) << (threadIdx.x & (32 - LANES));  // this group's lanes
-#pragma unroll
-  for (int o = 1; o < LANES; o <<= 1) mx = max(mx, __shfl_xor_sync(quad, mx, o));
-  const float amax = fmaxf(__uint_as_float(mx << 16), 1e-12f);
-  const float s = __fdiv_rn(amax, 448.0f);
-  const float r = __frcp_rn(s);
-  uint32_t code[kQuantVals / 4];  // 4 codes per word
-  float sum = 0.0f;
-#pragma unroll
-  for (int i = 0; i < kQuantVals / 8; ++i) {
-    uint32_t c[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t v = w[4 * i + j];
-      c[j] = e4m3x2(div_by_scale(bf16_lo(v), s, r), div_by_scale(bf16_hi(v), s, r));
-    }
-    if (gcorr) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t h2;
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(c[j])));
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-        sum += f.x + f.y;
-      }
-    }
-    code[2 * i] = c[0] | (c[1] << 16);
-    code[2 * i + 1] = c[2] | (c[3] << 16);
-  }
-  if (gcorr) {
-#pragma unroll
-    for (int o = 1; o < LANES; o <<= 1) sum += __shfl_xor_sync(quad, sum, o);
-  }
-  const float corr = -0.5f * __fmul_rn(s, sum);
+  uint32_t code[kQuantVals / 4];
+  float s, corr;
+  quantize_group<LANES>(x + row * K + g * kGroup, sub, gcorr != nullptr, code, s, corr);
   constexpr int kPre = 8;  // destinations fetched ahead (top-8 routing: all of them)
   for (int j0 = 0; j0 < k; j0 += kPre) {
     int64_t dst[kPre];
@@ -189,16 +174,7 @@ __global__ void __launch_bounds__(256)
     for (int j = 0; j < kPre; ++j) {
       const int64_t d = dst[j];  // the same for all of the group's lanes
       if (d < 0 || d >= M_out) continue;
-      uint8_t* qp = q + d * K + g * kGroup + sub * kQuantVals;
-      if constexpr (kQuantVals % 16 == 0) {  // 16-byte stores (the lane's bytes are 16-byte aligned)
-#pragma unroll
-        for (int i = 0; i < kQuantVals / 16; ++i)
-          reinterpret_cast<uint4*>(qp)[i] = make_uint4(code[4 * i], code[4 * i + 1], code[4 * i + 2], code[4 * i + 3]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < kQuantVals / 8; ++i)
-          reinterpret_cast<uint2*>(qp)[i] = make_uint2(code[2 * i], code[2 * i + 1]);
-      }
+      store_codes<LANES>(q + d * K + g * kGroup + sub * kQuantVals, code);
       if (sub == 0) {
         scales[g * ld + d] = s;
         if (gcorr) gcorr[g * ld + d] = corr;
@@ -295,9 +271,9 @@ extern "C" int fp8_quant_per_token_group(const uint16_t* x, int64_t M_src, int64
   W4A8_REQUIRE(scale_ld >= M_out && scale_ld % 4 == 0, "scale_ld must be >= M_out and a multiple of 4");
   if (M_out == 0) return W4A8_OK;
   W4A8_REQUIRE(x && q && scales, "null pointer");
-  W4A8_REQUIRE(((uintptr_t)x & 15) == 0 && ((uintptr_t)q & 7) == 0 && ((uintptr_t)scales & 3) == 0 &&
+  W4A8_REQUIRE(((uintptr_t)x & 15) == 0 && ((uintptr_t)q & 15) == 0 && ((uintptr_t)scales & 3) == 0 &&
                    ((uintptr_t)gcorr & 3) == 0,
-               "x must be 16-byte, q 8-byte and scales, gcorr 4-byte aligned");
+               "x and q must be 16-byte, scales and gcorr 4-byte aligned");
   const int64_t groups = M_out * (K / kGroup);
   const bool small = groups < kSmallLaunchGroups;
   const int64_t blocks = ceil_div(groups * (small ? 16 : 4), 256);
