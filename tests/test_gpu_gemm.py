@@ -135,3 +135,24 @@ def test_linear_split_k_needs_workspace(lib):
     with pytest.raises(lib.W4A8Error):
         lib.w4a8_linear(to_dev(aq), scales_to_gpu_layout(a_s), scales_to_gpu_layout(gcorr_of(aq, a_s)),
                         prepacked(lib, packed[0]), to_dev(ws[0]), ws=small)
+
+
+def test_tile_configurations_agree_bit_for_bit(lib):
+    # the same expert rows through the 16-wide tiles (few rows per expert), the 128-wide tiles (many) and
+    # the two-launch split (in between): each output element is the same fp32 sequence of per-group MMA
+    # partials and promotions, so the three give the same bf16 bits
+    rng = np.random.default_rng(77)
+    N, K, R = 256, 512, 10
+    aq0, as0 = _acts(rng, R, K)
+    big_q, big_s = _acts(rng, 300, K)
+    packed, ws = _weights(rng, 2, N, K)
+    outs = []
+    for other in (0, 300, 200):  # M = 10 (16-wide), 310 (128-wide), 210 (split: expert 0 on 16-wide tiles)
+        aq = np.concatenate([aq0, big_q[:other]])
+        a_s = np.concatenate([as0, big_s[:other]])
+        seg = np.array([0, R, R + other])
+        outs.append(_run_grouped(lib, aq, a_s, packed, ws, seg)[:R].cpu())
+    assert lib.device_error() == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    ref = _oracle_grouped(aq0, as0, packed, ws, np.array([0, R, R]))
+    assert rel_fro(f64_of_bf16(outs[0]), ref) <= 1e-3
