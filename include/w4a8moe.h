@@ -175,6 +175,11 @@ int fp8_quant_scatter_per_token_group(const uint16_t* x, int64_t T, int64_t K, c
  *   C bf16 [M_total][N]
  *   K % 128 == 0, N % 128 == 0, 1 <= E <= 1024, M_total < 2^31.
  * Rows outside every segment are not written.  ws may be NULL (none needed).
+ * The kernel configuration follows from the host-known M_total / E (the mean
+ * rows per expert) and K: up to 32, 16-row token tiles; from 128, 128-row
+ * tiles; in between, two kernel launches over disjoint experts (those with at
+ * most 16 rows on 16-row tiles, the others on 128-row tiles).  Every
+ * configuration computes each output element with the same fp32 operations.
  */
 int w4a8_grouped_gemm(const uint8_t* A, const float* a_scales, const float* a_gcorr,
                       int64_t a_scale_ld, const uint8_t* B_prepacked, const float* b_scales,
