@@ -519,9 +519,17 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
       const int mset = warp - kWarpMma;
       if (lane == 0) {
         uint32_t st = 0;
+        // the next tile's entry is loaded a tile ahead: a tile change costs the MMA issue no load latency
+        int4 nxt = sch.tiles && n_mine > 0 ? sch.tiles[0] : make_int4(0, 0, 0, 0);
         for (int item = blockIdx.x, it = 0; item < n_items; item += gridDim.x, ++it) {
           int e, nb, row0, rows;
-          sch.tile(it, item, e, nb, row0, rows);
+          if (sch.tiles) {
+            row0 = nxt.z;
+            rows = nxt.w;
+            if (it + 1 < n_mine) nxt = sch.tiles[it + 1];
+          } else {
+            sch.decode(item, e, nb, row0, rows);
+          }
           const int ncol = (row0 - (row0 & ~3) + rows + 15) & ~15;
           const uint32_t idesc = idesc_e4m3(static_cast<uint32_t>(ncol));
           int g_beg, g_end;
