@@ -1,12 +1,13 @@
 """Benchmark of the W4AFP8 MoE layer (and the dense W4AFP8 Linear) on GB300.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                [--workload decode|prefill|skewed|tiny|linear:M,N,K]
+                [--workload decode|prefill|skewed|tiny|moe:T,H,I,E,k|ep:<workload>:R:r|linear:M,N,K]
 
 One step = one pass of the whole hot path over one batch of synthetic input:
-routing -> permutation -> FP8 quantisation (gathered) -> w13 grouped GEMM ->
-SiLU-and-Mul requantisation -> w2 grouped GEMM -> combine, all through the C
-ABI.  Prints one JSON line (rank 0).  Default workload: the DeepSeek-V3/R1-
+routing -> permutation -> FP8 quantisation (each token's row scattered to its
+routed places) -> w13 grouped GEMM -> SiLU-and-Mul requantisation -> w2 grouped
+GEMM -> combine, all through the C ABI (ep:...: one expert-parallel shard, the
+pairs of experts r, r+R, ... only).  Prints one JSON line (rank 0).  Default workload: the DeepSeek-V3/R1-
 shaped decode layer (T=64, H=7168, I=2048, E=256, top-8), weights 6.0 GB
 (larger than L2, so every step streams them from HBM).
 
