@@ -42,7 +42,18 @@
 //     expert's rows on a grid of NMAX rows that starts at its first row rounded
 //     down to a multiple of 4 (so scale vectors stay 16-byte aligned); the schedule is built
 //     in shared memory from seg_indptr by every CTA (no host synchronisation,
-//     no workspace), and CTAs stride over it.
+//     no workspace), and CTAs stride over it.  Each CTA decodes its own tiles
+//     once, in the prologue, into a shared-memory list that every role reads.
+//   * Wide token tiles (128) promote from 16x256b tensor-memory fragments (4 rows
+//     x 16 columns per thread, so a token scale read serves 4 rows) and move
+//     registers from the producer/MMA and converter warpgroups to the epilogue
+//     warpgroups with setmaxnreg.
+//   * Configurations (host side, from the mean rows per expert and K): 16-wide
+//     token tiles with 4 groups per stage for few rows per expert (4 MMA warps
+//     for long K), 128-wide tiles with 2 groups per stage and the converted
+//     weights in shared memory for many, both in two launches over disjoint
+//     experts in between; split-K with fp32 partials for dense Linear calls
+//     whose tiles leave SMs idle.
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
