@@ -71,9 +71,10 @@ int w4a8_abi_version(void);
 
 /*
  * Reads and clears the device-side error word of the current device
- * (synchronises the device).  Non-zero means a kernel's bounded wait on an
+ * (synchronises the device).  Bit 0 (1): a kernel's bounded wait on an
  * mbarrier gave up (W4A8_ERR_TIMEOUT) and that kernel's outputs are invalid.
- * For tests and diagnostics, not for the hot path.
+ * Bit 1 (2): a routed expert id or an expert_map entry was out of range and
+ * those pairs were left out.  For tests and diagnostics, not for the hot path.
  */
 int w4a8_device_error(void);
 
