@@ -32,13 +32,14 @@ int check_launch(const char* what) {
 }
 
 int num_sms() {
+  constexpr int kGb300Sms = 152;  // used only if the device cannot be queried
   static int cache[64] = {0};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kGb300Sms;
   if (!cache[dev]) {
     int n = 0;
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cache[dev] = n > 0 ? n : 148;
+    cache[dev] = n > 0 ? n : kGb300Sms;
   }
   return cache[dev];
 }
