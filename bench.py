@@ -139,13 +139,15 @@ class ClockSampler:
                 rows.append(parts)
         if not rows:
             return None
-        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        def num(v):  # nvidia-smi prints "[N/A]" for a field it cannot read
+            return float(v) if v.replace(".", "", 1).isdigit() else None
+
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[4]) for r in rows if num(r[4]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.lower() == "active"})
-        return {"sm_mhz": float(np.median(sm)) if sm else None,
-                "sm_max_mhz": float(rows[0][3]) if rows[0][3].replace(".", "").isdigit() else None,
-                "power_w_max": max(float(r[4]) for r in rows if r[4].replace(".", "").isdigit()),
-                "samples": len(rows), "reasons": reasons}
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": num(rows[0][3]),
+                "power_w_max": max(pw) if pw else None, "samples": len(rows), "reasons": reasons}
 
 
 def device_uuid(dev):
@@ -195,6 +197,51 @@ def reduce_max(value: float, device) -> float:
 def throughput(units_per_rank: float, world: int, max_ms: float) -> float:
     """Whole-job throughput: units processed by all ranks / the slowest rank's time."""
     return world * units_per_rank / (max_ms / 1e3)
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work and rooflines (host arithmetic only)
+
+def moe_counts(T, H, I, E, k, P, n_touched):
+    """Algorithmic work of one MoE layer step over P routed pairs, n_touched of the E experts holding any.
+
+    FLOPs count the routed pairs only (no padding).  Bytes count the int4 weights and fp32 per-128 scales of
+    the touched experts once, plus x and the router logits read and the output written.  The w13 launch
+    reads its experts' weights and scales, the pairs' E4M3 codes and per-128 scales, and writes Y13 in bf16.
+    """
+    w13_w = n_touched * (2 * I * H // 2 + 2 * I * (H // 128) * 4)
+    w2_w = n_touched * (H * I // 2 + H * (I // 128) * 4)
+    return {"flops": 2.0 * P * (2 * I * H + I * H),
+            "layer_bytes": w13_w + w2_w + T * H * 2 + T * E * 4 + T * H * 2,
+            "w13_bytes": w13_w + P * H + (H // 128) * P * 4 + P * 2 * I * 2,
+            "w13_flops": 2.0 * P * 2 * I * H}
+
+
+def linear_counts(M, N, K):
+    """Algorithmic work of one dense W4AFP8 Linear call: int4 weights + fp32 scales, E4M3 codes + scales of
+    the M rows, bf16 output."""
+    G = K // 128
+    return {"flops": 2.0 * M * N * K, "bytes": N * K // 2 + N * G * 4 + M * K + M * G * 4 + M * N * 2}
+
+
+def moe_launches_per_step(n_stages, two_pass_permute, pairs, experts):
+    """Kernels one layer step launches: one per stage, plus the permutation's count pass from 8192 pairs,
+    plus a second launch of each grouped GEMM when the mean rows per expert lie strictly between 32 and
+    128 (experts with at most 16 rows on the narrow tiles, the rest on the wide ones)."""
+    return n_stages + (1 if two_pass_permute else 0) + (2 if 32 * experts < pairs < 128 * experts else 0)
+
+
+def roofline_core(alg_bytes, flops, ms, hbm_gbs, tensor_tflops):
+    """The bound that applies (the larger of bytes / bandwidth and FLOPs / peak) and the fraction of it that
+    one launch of `ms` milliseconds reaches."""
+    sec = ms / 1e3
+    if alg_bytes / (hbm_gbs * 1e9) >= flops / (tensor_tflops * 1e12):
+        ach = alg_bytes / sec / 1e9
+        return {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_gbs, "unit": "GB/s",
+                "frac": round(ach / hbm_gbs, 4)}
+    ach = flops / sec / 1e12
+    return {"bound": "tensor", "achieved": round(ach, 1), "peak": tensor_tflops, "unit": "TFLOP/s",
+            "frac": round(ach / tensor_tflops, 4)}
 
 
 # ---------------------------------------------------------------------------
@@ -385,29 +432,17 @@ def run_ours(args, name, cfg):
     P = int(seg[-1])  # routed pairs computed (all T*k, or the shard's)
     ms_step = ms / K
     value = throughput(T * K, world, ms)
-    flops = 2.0 * P * (2 * I * H + I * H)
-    w13_bytes = n_touched * (2 * I * H // 2 + 2 * I * (H // 128) * 4)
-    w2_bytes = n_touched * (H * I // 2 + H * (I // 128) * 4)
-    layer_bytes = w13_bytes + w2_bytes + T * H * 2 + T * E * 4 + T * H * 2
-    # dominant kernel: the w13 grouped GEMM
-    w13_ms = w13_timed_ms
-    w13_alg_bytes = w13_bytes + P * H + (H // 128) * P * 4 + P * 2 * I * 2
-    w13_flops = 2.0 * P * 2 * I * H
-    hbm_bound = (w13_alg_bytes / (peaks["hbm_gbs"] * 1e9)) >= (w13_flops / (FP8_OVER_BF16 * peaks["bf16_tflops_sustained"] * 1e12))
-    traffic = ncu_traffic(f"{name}:w13")
-    if hbm_bound:
-        ach = w13_alg_bytes / (w13_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic,
-                "kernel": "w4a8_gemm_kernel (w13 grouped GEMM)",
-                "algorithmic_bytes": int(w13_alg_bytes), "peak_source": f"{peak_src} hbm_gbs"}
+    cnt = moe_counts(T, H, I, E, k, P, n_touched)
+    flops, layer_bytes = cnt["flops"], cnt["layer_bytes"]
+    # dominant kernel: the w13 grouped GEMM, timed inside the long step (sustained tensor peak)
+    roof = roofline_core(cnt["w13_bytes"], cnt["w13_flops"], w13_timed_ms, peaks["hbm_gbs"],
+                         FP8_OVER_BF16 * peaks["bf16_tflops_sustained"])
+    roof.update({"traffic": ncu_traffic(f"{name}:w13"), "kernel": "w4a8_gemm_kernel (w13 grouped GEMM)"})
+    if roof["bound"] == "hbm":
+        roof.update({"algorithmic_bytes": int(cnt["w13_bytes"]), "peak_source": f"{peak_src} hbm_gbs"})
     else:
-        pk = FP8_OVER_BF16 * peaks["bf16_tflops_sustained"]
-        ach = w13_flops / (w13_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": pk, "unit": "TFLOP/s",
-                "frac": round(ach / pk, 4), "traffic": traffic, "kernel": "w4a8_gemm_kernel (w13 grouped GEMM)",
-                "algorithmic_flops": w13_flops,
-                "peak_source": f"{peak_src} bf16_tflops_sustained x 2 (nominal fp8/bf16 dense ratio)"}
+        roof.update({"algorithmic_flops": cnt["w13_flops"],
+                     "peak_source": f"{peak_src} bf16_tflops_sustained x 2 (nominal fp8/bf16 dense ratio)"})
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
@@ -428,9 +463,7 @@ def run_ours(args, name, cfg):
         "stages_note": "stage breakdown from a separate pass with an event after every stage; the timed "
                        "region runs the stages back to back with events only around w13",
         "roofline": roof,
-        # the permutation is two kernels (count + placement) from 8192 routed pairs; with 32 to 128 rows per
-        # expert on average each grouped GEMM is two kernels (experts up to 16 rows, then the rest)
-        "gpu_launches": (nst + (1 if r.permute_ws_bytes else 0) + (2 if 32 * r.EL < T * k < 128 * r.EL else 0)) * K,
+        "gpu_launches": moe_launches_per_step(nst, r.permute_ws_bytes > 0, T * k, r.EL) * K,
         "clocks": clk.summary(),
     }
     if not args.no_e2e:
@@ -508,15 +541,10 @@ def run_linear(args, cfg, dev, world, rank, peaks, peak_src):
         torch.cuda.synchronize(dev)
     ms = evs[0].elapsed_time(evs[-1])
     ms_step = ms / Kst
-    flops = 2.0 * M * N * K
-    byts = N * K // 2 + N * G * 4 + M * K + M * G * 4 + M * N * 2
-    hbm = byts / (ms_step / 1e3) / 1e9
-    tf = flops / (ms_step / 1e3) / 1e12
-    pk_t = FP8_OVER_BF16 * peaks["bf16_tflops"]
-    bound = "hbm" if byts / (peaks["hbm_gbs"] * 1e9) >= flops / (pk_t * 1e12) else "tensor"
-    roof = ({"bound": "hbm", "achieved": round(hbm, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-             "frac": round(hbm / peaks["hbm_gbs"], 4)} if bound == "hbm" else
-            {"bound": "tensor", "achieved": round(tf, 1), "peak": pk_t, "unit": "TFLOP/s", "frac": round(tf / pk_t, 4)})
+    cnt = linear_counts(M, N, K)
+    tf = cnt["flops"] / (ms_step / 1e3) / 1e12
+    # a call timed alone: the burst tensor peak
+    roof = roofline_core(cnt["bytes"], cnt["flops"], ms_step, peaks["hbm_gbs"], FP8_OVER_BF16 * peaks["bf16_tflops"])
     roof.update({"traffic": ncu_traffic(f"linear:{M},{N},{K}"),
                  "kernel": "w4a8_gemm_kernel (dense; per call, incl. the split-K reduce when S > 1)",
                  "peak_source": peak_src})
