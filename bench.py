@@ -8,8 +8,10 @@ routing -> permutation -> FP8 quantisation (each token's row scattered to its
 routed places) -> w13 grouped GEMM -> SiLU-and-Mul requantisation -> w2 grouped
 GEMM -> combine, all through the C ABI (ep:...: one expert-parallel shard, the
 pairs of experts r, r+R, ... only).  Prints one JSON line (rank 0).  Default workload: the DeepSeek-V3/R1-
-shaped decode layer (T=64, H=7168, I=2048, E=256, top-8), weights 6.0 GB
-(larger than L2, so every step streams them from HBM).
+shaped prefill layer (T=8192, H=7168, I=2048, E=256, top-8; 5.77 TFLOP per step, reported against the
+FP8 tensor roofline), weights 6.0 GB (larger than L2, so every step streams them from HBM).  The same
+line carries the decode layer (T=64, same experts, against the HBM roofline) under "decode", measured in
+the same process on the same weights.
 
 --impl reference times the CPU oracle (numpy, float64, one thread) on a bounded
 sample of the same workload (a few tokens per step).
@@ -48,10 +50,13 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--workload", default="prefill")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="prefill: leave out the decode layer's keys")
+    ap.add_argument("--sustain-s", type=float, default=1.5,
+                    help="seconds of untimed steps after the timed region with the clocks sampled (0: none)")
     ap.add_argument("--cpu-tokens", type=int, default=0, help="tokens per oracle step (0: automatic)")
     return ap.parse_args()
 
@@ -148,6 +153,80 @@ class ClockSampler:
         reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.lower() == "active"})
         return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": num(rows[0][3]),
                 "power_w_max": max(pw) if pw else None, "samples": len(rows), "reasons": reasons}
+
+
+class NvmlSampler:
+    """SM clock, power and clock-event reasons read through NVML (libnvidia-ml, read-only queries) every
+    `period_s` seconds on a background thread while the timed region runs; summary() as ClockSampler's."""
+
+    # clock-event reason bits of nvmlDeviceGetCurrentClocksEventReasons
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_slowdown"}
+
+    def __init__(self, uuid, period_s=0.01, nvml=None):
+        import ctypes
+        self.uuid, self.period_s = uuid, period_s
+        self.rows = []
+        self.nv = nvml if nvml is not None else ctypes.CDLL("libnvidia-ml.so.1")
+        if self.nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if not uuid or self.nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle for the device")
+        self.reasons_fn = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.max_mhz = self._uint(self.nv.nvmlDeviceGetMaxClockInfo, 1)
+
+    def _uint(self, fn, *args):
+        import ctypes
+        v = ctypes.c_uint()
+        return v.value if fn(self.h, *args, ctypes.byref(v)) == 0 else None
+
+    def sample(self):
+        import ctypes
+        r = ctypes.c_ulonglong()
+        reasons = r.value if self.reasons_fn(self.h, ctypes.byref(r)) == 0 else 0
+        pw = self._uint(self.nv.nvmlDeviceGetPowerUsage)
+        self.rows.append((self._uint(self.nv.nvmlDeviceGetClockInfo, 1), None if pw is None else pw / 1e3,
+                          reasons))
+
+    def _loop(self):
+        while not self.stop.wait(self.period_s):
+            self.sample()
+
+    def __enter__(self):
+        import threading
+        self.stop = threading.Event()
+        self.sample()
+        self.th = threading.Thread(target=self._loop, daemon=True)
+        self.th.start()
+        return self
+
+    def __exit__(self, *a):
+        self.stop.set()
+        self.th.join()
+        self.sample()
+
+    def summary(self):
+        return summarize_clock_rows(self.rows, self.max_mhz, self.REASONS)
+
+
+def summarize_clock_rows(rows, max_mhz, reason_bits):
+    """Median SM clock, peak power and the throttle reasons seen in (sm_mhz, power_w, reason bitmask) rows."""
+    sm = [r[0] for r in rows if r[0] is not None]
+    pw = [r[1] for r in rows if r[1] is not None]
+    reasons = sorted({name for r in rows for bit, name in reason_bits.items() if r[2] & bit})
+    return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max_mhz,
+            "power_w_max": max(pw) if pw else None, "samples": len(rows), "reasons": reasons,
+            "source": "NVML every 10 ms"}
+
+
+def clock_sampler(dev):
+    """NVML sampler when libnvidia-ml answers, else nvidia-smi every 200 ms."""
+    try:
+        return NvmlSampler(device_uuid(dev))
+    except (OSError, AttributeError):
+        return ClockSampler(device_uuid(dev))
 
 
 def device_uuid(dev):
@@ -250,7 +329,7 @@ def roofline_core(alg_bytes, flops, ms, hbm_gbs, tensor_tflops):
 class MoeRunner:
     """Device buffers of one MoE layer and the seven C-ABI calls of one step."""
 
-    def __init__(self, cfg, seed, dev):
+    def __init__(self, cfg, seed, dev, weights=None):
         import torch
 
         import w4afp8_mixture_experts_gb300 as m
@@ -260,11 +339,15 @@ class MoeRunner:
         self.cfg = cfg
         T, H, I, E, k = (cfg[x] for x in ("T", "H", "I", "E", "k"))
         self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
-        # weights are prepacked once after generation (the post-load processing step), untimed
-        self.w13 = m.w4a8_prepack_weights(inputs.gpu_packed_int4(seed, inputs.STREAM_W13, (E, 2 * I, H // 2), dev))
-        self.w13s = inputs.gpu_scales(seed, inputs.STREAM_W13_SCALE, (E, H // 128, 2 * I), dev)
-        self.w2 = m.w4a8_prepack_weights(inputs.gpu_packed_int4(seed, inputs.STREAM_W2, (E, H, I // 2), dev))
-        self.w2s = inputs.gpu_scales(seed, inputs.STREAM_W2_SCALE, (E, I // 128, H), dev)
+        if weights is not None:  # another workload's experts of the same shape (same seed)
+            self.w13, self.w13s, self.w2, self.w2s = weights
+        else:
+            # weights are prepacked once after generation (the post-load processing step), untimed
+            self.w13 = m.w4a8_prepack_weights(inputs.gpu_packed_int4(seed, inputs.STREAM_W13, (E, 2 * I, H // 2),
+                                                                     dev))
+            self.w13s = inputs.gpu_scales(seed, inputs.STREAM_W13_SCALE, (E, H // 128, 2 * I), dev)
+            self.w2 = m.w4a8_prepack_weights(inputs.gpu_packed_int4(seed, inputs.STREAM_W2, (E, H, I // 2), dev))
+            self.w2s = inputs.gpu_scales(seed, inputs.STREAM_W2_SCALE, (E, I // 128, H), dev)
         self.ep = cfg.get("ep")
         self.EL = E
         self.emap = None
@@ -377,6 +460,56 @@ def run_ours(args, name, cfg):
     if name == "linear":
         return run_linear(args, cfg, dev, world, rank, peaks, peak_src)
     r = MoeRunner(cfg, seed, dev)
+    res = measure_moe(r, name, cfg, args, dev, world, peaks, peak_src)
+    if not args.no_e2e:
+        res["e2e"] = e2e_moe(r, args, dev, world)
+    if name == "prefill" and not args.no_decode:
+        # the decode half of the metric: the same experts (same seed, same tensors), 64 tokens
+        dcfg = dict(inputs.WORKLOADS["decode"])
+        rd = MoeRunner(dcfg, seed, dev, weights=(r.w13, r.w13s, r.w2, r.w2s))
+        d = measure_moe(rd, "decode", dcfg, args, dev, world, peaks, peak_src)
+        keep = ("value", "unit", "ms_per_step", "steps", "tflops", "layer_roofline", "stages_ms", "roofline",
+                "gpu_launches", "clocks")
+        res["decode"] = {"workload": d["config"]["workload"], "experts_touched": d["config"]["experts_touched"],
+                         **{kk: d[kk] for kk in keep}}
+        if not args.no_e2e:
+            res["decode"]["e2e"] = e2e_moe(rd, args, dev, world)
+    res["clocks_sustained"] = sustained_clocks(r, dev, args.sustain_s)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(name, args.workload, args)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+def sustained_clocks(r, dev, seconds):
+    """Steps back to back for about `seconds` after the timed region (untimed), with the clocks sampled:
+    the clock and power state of the GPU under this workload's sustained load."""
+    import torch
+    if seconds <= 0:
+        return None
+    stream = torch.cuda.current_stream(dev)
+    st = r.stages(stream.cuda_stream)
+    t = time.perf_counter()
+    with clock_sampler(dev) as clk:
+        n = 0
+        while time.perf_counter() - t < seconds:
+            for _ in range(10):
+                for nm, fn in st:
+                    if fn():
+                        raise RuntimeError(f"{nm}: {r.lib.w4a8_last_error().decode()}")
+            n += 10
+            torch.cuda.synchronize(dev)
+    out = clk.summary() or {}
+    out["steps"] = n
+    return out
+
+
+def measure_moe(r, name, cfg, args, dev, world, peaks, peak_src):
+    """W warm-up steps, then exactly K timed steps of the seven stages back to back; the result line."""
+    import torch
+    import torch.distributed as dist
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
     st = r.stages(sp)
@@ -401,7 +534,7 @@ def run_ours(args, name, cfg):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(device_uuid(dev)) as clk:
+    with clock_sampler(dev) as clk:
         t0.record(stream)
         for i in range(K):
             for j, (nm, fn) in enumerate(st):
@@ -443,7 +576,7 @@ def run_ours(args, name, cfg):
     else:
         roof.update({"algorithmic_flops": cnt["w13_flops"],
                      "peak_source": f"{peak_src} bf16_tflops_sustained x 2 (nominal fp8/bf16 dense ratio)"})
-    res = {
+    return {
         "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3 x int4 -> f32 (bf16 out)", "data": "synthetic",
@@ -466,14 +599,6 @@ def run_ours(args, name, cfg):
         "gpu_launches": moe_launches_per_step(nst, r.permute_ws_bytes > 0, T * k, r.EL) * K,
         "clocks": clk.summary(),
     }
-    if not args.no_e2e:
-        res["e2e"] = e2e_moe(r, args, dev, world)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(name, args.workload, args)
-    if world > 1:
-        dist.destroy_process_group()
-    if rank == 0:
-        print(json.dumps(res), flush=True)
 
 
 def e2e_moe(r, args, dev, world):
@@ -531,7 +656,7 @@ def run_linear(args, cfg, dev, world, rank, peaks, peak_src):
     # events only around the K calls: the calls are launched back to back, as a model would, so a
     # call's launch and prologue overlap the previous call (programmatic dependent launch)
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    with ClockSampler(device_uuid(dev)) as clk:
+    with clock_sampler(dev) as clk:
         evs[0].record()
         for i in range(Kst):
             rc = step(i)

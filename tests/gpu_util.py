@@ -4,7 +4,7 @@ import torch
 
 
 def dev():
-    return torch.device("cuda:0")
+    return torch.device("cuda", torch.cuda.current_device())
 
 
 def bf16_from_bits(bits):

@@ -182,3 +182,54 @@ def test_default_cpu_sample_sizes():
     assert bench.default_cpu_tokens("decode") == 1
     assert bench.default_cpu_tokens("ep-prefill") == 8
     assert np.isfinite(bench.throughput(1, 1, 1.0))
+
+
+class _FakeNvml:
+    """Stands in for libnvidia-ml: fixed clocks and power, a reason bitmask that changes per call."""
+
+    def __init__(self, reasons):
+        self.reasons = list(reasons)
+        self.calls = 0
+
+    def nvmlInit_v2(self):
+        return 0
+
+    def nvmlDeviceGetHandleByUUID(self, uuid, handle):
+        return 0 if uuid == b"GPU-x" else 1
+
+    def nvmlDeviceGetMaxClockInfo(self, h, kind, out):
+        out._obj.value = 2070
+        return 0
+
+    def nvmlDeviceGetClockInfo(self, h, kind, out):
+        out._obj.value = 1900 + 10 * (self.calls % 3)
+        return 0
+
+    def nvmlDeviceGetPowerUsage(self, h, out):
+        out._obj.value = 1200000 + 1000 * self.calls
+        return 0
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h, out):
+        out._obj.value = self.reasons[self.calls % len(self.reasons)]
+        self.calls += 1
+        return 0
+
+
+def test_nvml_sampler_with_a_fake_library():
+    fake = _FakeNvml([0x0, 0x4, 0x1])  # idle and power cap bits; idle is not a throttle reason
+    s = bench.NvmlSampler("GPU-x", period_s=0.001, nvml=fake)
+    with s:
+        pass
+    out = s.summary()
+    assert out["sm_max_mhz"] == 2070 and out["samples"] >= 2
+    assert out["reasons"] == (["sw_power_cap"] if out["samples"] >= 2 else [])
+    assert 1900 <= out["sm_mhz"] <= 1920 and out["power_w_max"] >= 1200.0
+    with pytest.raises(OSError):
+        bench.NvmlSampler("GPU-other", nvml=_FakeNvml([0]))
+
+
+def test_clock_rows_summary_names_the_rejecting_reasons():
+    rows = [(2070, 900.0, 0x0), (1800, 1400.0, 0x8 | 0x4), (1500, 1390.0, 0x40), (None, None, 0x20)]
+    out = bench.summarize_clock_rows(rows, 2070, bench.NvmlSampler.REASONS)
+    assert out["sm_mhz"] == 1800 and out["power_w_max"] == 1400.0 and out["samples"] == 4
+    assert out["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_power_cap", "sw_thermal_slowdown"]

@@ -156,3 +156,45 @@ def test_tile_configurations_agree_bit_for_bit(lib):
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
     ref = _oracle_grouped(aq0, as0, packed, ws, np.array([0, R, R]))
     assert rel_fro(f64_of_bf16(outs[0]), ref) <= 1e-3
+
+
+# The dense Linear sweep at its own shapes: M in {1, 16, 128, 1024, 8192} x (N, K) in {(24576, 1536),
+# (7168, 16384), (18432, 7168), (7168, 2048)}, with the bench's weights (counter-based generator, filled
+# on the device) and x ~ N(0,1) quantised by the library.  Every row up to M = 128 and a seeded sample of
+# 64 rows (first and last included) above is compared with the oracle at 1e-3 relative Frobenius per
+# shape; the sampled rows' codes and scales must equal the oracle's quantisation bit for bit.
+@pytest.mark.parametrize("N,K", inputs.LINEAR_NK)
+def test_linear_sweep_shapes(lib, N, K):
+    from gpu_util import bf16_from_bits, scales_from_gpu_layout
+    seed, G = 0, K // 128
+    W = lib.w4a8_prepack_weights(inputs.gpu_packed_int4(seed, inputs.STREAM_LIN_W, (N, K // 2)))
+    S = inputs.gpu_scales(seed, inputs.STREAM_LIN_SCALE, (G, N))
+    got, codes, scales, spans = [], [], [], []
+    for M in inputs.LINEAR_M:
+        rng = np.random.default_rng(1000 + M)
+        x_bits = inputs.to_bf16_bits(rng.standard_normal((M, K), dtype=np.float32))
+        aq, a_s, a_c = lib.fp8_quant_per_token_group(bf16_from_bits(x_bits))
+        C = lib.w4a8_linear(aq, a_s, a_c, W, S)
+        if M <= 128:
+            sel = np.arange(M)
+        else:
+            sel = np.sort(np.concatenate([[0, M - 1], rng.choice(np.arange(1, M - 1), 62, replace=False)]))
+        idx = torch.from_numpy(sel).cuda()
+        got.append(f64_of_bf16(C.index_select(0, idx)))
+        rq, rs = oracle.quant_per_token_group(inputs.bf16_bits_to_f32(x_bits[sel]))
+        assert np.array_equal(aq.index_select(0, idx).cpu().numpy(), rq)
+        assert np.array_equal(scales_from_gpu_layout(a_s, M)[sel], rs)
+        codes.append(rq)
+        scales.append(rs)
+        spans.append((M, len(sel)))
+        assert lib.device_error() == 0
+    Wh = oracle.unpack_int4(inputs.packed_int4(seed, inputs.STREAM_LIN_W, 0, N * K // 2).reshape(N, K // 2))
+    Sh = np.ascontiguousarray(inputs.scales(seed, inputs.STREAM_LIN_SCALE, 0, G * N).reshape(G, N).T)
+    ref = oracle.linear(np.concatenate(codes), np.concatenate(scales), Wh, Sh)
+    o = 0
+    for (M, n), g in zip(spans, got):
+        err = rel_fro(g, ref[o:o + n])
+        print(f"Linear M={M} N={N} K={K} (split-K {lib.linear_workspace_bytes(M, N, K) // (4 * M * N) or 1}): "
+              f"{n} rows, rel Frobenius {err:.2e}")
+        assert err <= 1e-3, (M, err)
+        o += n

@@ -124,20 +124,80 @@ def test_layer_zero_and_huge_rows(lib):
     assert rel_fro(got, ref) <= 2e-2
 
 
-@pytest.mark.parametrize("name,sample", [("decode", [0, 17, 63]), ("prefill", [0, 4095]),
-                                         ("skewed", [0, 2048])])
-def test_full_size_sampled_tokens(lib, name, sample):
+# Full-size workloads in the bench's launch configuration.  decode: every token; prefill and skewed: a
+# seeded sample of 256 tokens holding the first and last token (and, for the skewed routing, tokens of the
+# hottest expert and of the nearly empty ones).  For every routed pair of a sampled token the device's
+# Y13 and Y2 rows are compared with the oracle's GEMM of the same rows at the stage tolerance (1e-3), its
+# Hq codes with the oracle's requantisation of its Y13 (the c15 gate), and the layer output with the
+# oracle's own chain at the end-to-end tolerance (2e-2).  Routing ids and the permutation are compared
+# for all tokens, bit for bit.
+@pytest.mark.parametrize("name,n", [("decode", 64), ("prefill", 256), ("skewed", 256)])
+def test_full_size_sampled_tokens(lib, name, n):
+    import fullsize
     cfg = inputs.WORKLOADS[name]
+    T, H, I, E, k = (cfg[c] for c in ("T", "H", "I", "E", "k"))
+    P = T * k
     out, ws, L, x_bits, logits = _run_layer(lib, 0, cfg)
-    w13h, w2h = moe_experts(0, cfg)
     x = inputs.bf16_bits_to_f32(x_bits)
-    got = f64_of_bf16(out)[sample]
-    ref, ids, _ = oracle.moe_tokens(x[sample], logits[sample], cfg["k"], w13h.w, w13h.s, w2h.w, w2h.s)
-    err = rel_fro(got, ref)
-    print(f"{name}: sampled tokens {sample}: rel Frobenius {err:.2e}, max abs {np.abs(got - ref).max():.3e}")
-    assert err <= 2e-2
-    # invariants over every token: finite, routing ids exact for all tokens
     allout = f64_of_bf16(out)
     assert np.all(np.isfinite(allout))
-    rid, _ = oracle.route_topk(logits, cfg["k"])
-    assert np.array_equal(_ws_view(ws, L.topk_ids, torch.int32, (cfg["T"], cfg["k"])).numpy(), rid)
+    rid, _ = oracle.route_topk(logits, k)
+    assert np.array_equal(_ws_view(ws, L.topk_ids, torch.int32, (T, k)).numpy(), rid)
+    rseg, rs2d, rd2s = oracle.permute(rid, E)
+    seg = _ws_view(ws, L.seg_indptr, torch.int64, (E + 1,)).numpy()
+    s2d = _ws_view(ws, L.src2dst, torch.int32, (P,)).numpy()
+    d2s = _ws_view(ws, L.dst2src, torch.int32, (P,)).numpy()
+    assert np.array_equal(seg, rseg) and np.array_equal(s2d, rs2d) and np.array_equal(d2s, rd2s)
+    extra = ()
+    if cfg.get("zipf"):
+        extra, hot, cold = fullsize.skew_extremes(rid, E)
+        counts = np.diff(seg)
+        print(f"{name}: hottest expert {hot} ({counts[hot]} rows), coldest used {cold} "
+              f"({counts[cold].tolist()} rows), {np.count_nonzero(counts == 0)} empty experts")
+    sample = fullsize.pick_tokens(T, max(n, len(extra) + 2), 1234, rid, E, extra)
+    pairs = (sample[:, None] * k + np.arange(k)[None, :]).reshape(-1)
+    r_idx = torch.from_numpy(s2d[pairs].astype(np.int64)).cuda()
+    ld = L.scale_ld
+
+    def rows_of(off, dtype, width):
+        n_el = P * width
+        t = ws[off:off + n_el * torch.tensor([], dtype=dtype).element_size()].view(dtype).view(P, width)
+        return t.index_select(0, r_idx).cpu()
+
+    def scale_rows(off, G):
+        t = ws[off:off + G * ld * 4].view(torch.float32).view(G, ld)
+        return t.index_select(1, r_idx).t().contiguous().cpu().numpy()
+
+    rows = dict(xq=rows_of(L.xq, torch.uint8, H).numpy(), xs=scale_rows(L.xs, H // 128),
+                y13=rows_of(L.y13, torch.bfloat16, 2 * I).float().numpy().astype(np.float64),
+                hq=rows_of(L.hq, torch.uint8, I).numpy(), hs=scale_rows(L.hs, I // 128),
+                y2=rows_of(L.y2, torch.bfloat16, H).float().numpy().astype(np.float64))
+    # quantised rows of the sampled pairs: exact against the oracle's quantisation of the tokens
+    rq, rs = oracle.quant_per_token_group(x[sample])
+    tok = np.repeat(np.arange(sample.size), k)
+    assert np.array_equal(rows["xq"], rq[tok]) and np.array_equal(rows["xs"], rs[tok])
+    stats, out_ref = fullsize.sampled_layer_check(0, cfg, sample, logits, rows)
+    got = allout[sample]
+    err = rel_fro(got, out_ref)
+    print(f"{name}: {sample.size} tokens ({pairs.size} pairs): w13 {stats['y13']:.2e}, w2 {stats['y2']:.2e}, "
+          f"SiLU codes differing {stats['hq_mismatch']:.2e} (dequantised {stats['hq_deq']:.2e}), "
+          f"end to end {err:.2e}, max abs {np.abs(got - out_ref).max():.3e}")
+    assert stats["y13"] <= 1e-3 and stats["y2"] <= 1e-3
+    assert stats["hq_mismatch"] <= 1e-3 and stats["hq_deq"] <= 1e-3
+    assert err <= 2e-2
+    assert lib.device_error() == 0
+
+
+def test_layer_on_a_second_device(lib):
+    # Launch attributes (the GEMM's and permutation's shared-memory limits) are per device: the layer must
+    # also run on a device other than the first one the process used.
+    if torch.cuda.device_count() < 2:
+        pytest.skip("one CUDA device")
+    cfg = dict(T=300, H=256, I=256, E=4, k=2)
+    x_bits, logits = moe_host_inputs(4, cfg)
+    w13h, w2h = moe_experts(4, cfg)
+    ref = oracle.moe_layer(inputs.bf16_bits_to_f32(x_bits), logits, 2, w13h.w, w13h.s, w2h.w, w2h.s)["out"]
+    for d in (0, 1):
+        with torch.cuda.device(d):
+            out, _, _, _, _ = _run_layer(lib, 4, cfg, x_bits, logits)
+            assert rel_fro(f64_of_bf16(out), ref) <= 2e-2

@@ -6,6 +6,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/w4a8moe.h"
 
 namespace w4a8 {
@@ -39,6 +42,29 @@ inline int launch_pdl(const char* what, void (*kernel)(KArgs...), dim3 grid, dim
   do {                                                           \
     if (!(cond)) return ::w4a8::set_error(W4A8_ERR_INVALID_ARG, __VA_ARGS__); \
   } while (0)
+
+// Host-side set-up that must happen once per device (function attributes are per device): run(f)
+// calls f() under a lock the first time on the current device and records success; later calls
+// on that device return W4A8_OK without calling f.  Devices 0..63; beyond that f runs every time.
+class DeviceOnce {
+ public:
+  template <class F>
+  int run(F&& f) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return f();
+    const uint64_t bit = 1ull << dev;
+    if (done_.load(std::memory_order_acquire) & bit) return W4A8_OK;
+    std::lock_guard<std::mutex> lk(mu_);
+    if (done_.load(std::memory_order_relaxed) & bit) return W4A8_OK;
+    const int rc = f();
+    if (rc == W4A8_OK) done_.fetch_or(bit, std::memory_order_release);
+    return rc;
+  }
+
+ private:
+  std::atomic<uint64_t> done_{0};
+  std::mutex mu_;
+};
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }

@@ -70,8 +70,8 @@ constexpr int kWarpTmaAct = 1;               // producer of the token and scale 
 constexpr int kWarpMma = 2;                  // warps 2 .. 1 + kMmaWarps issue the MMAs
 constexpr int kConvWarps = 4;                // converter warps per set: one per tensor-memory lane quarter
 constexpr int kMaxExperts = 1024;
-constexpr int kMaxDynSmem = 227 * 1024;
-constexpr int kSmallExpertRows = 16;  // grouped GEMM with many rows: experts up to this many rows take 16-wide tiles  // dynamic shared memory a CTA may use on sm_100 / sm_103
+constexpr int kMaxDynSmem = 227 * 1024;  // dynamic shared memory a CTA may use on sm_100 / sm_103
+constexpr int kSmallExpertRows = 16;  // grouped GEMM with many rows: experts up to this many rows take 16-wide tiles
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s: no legitimate wait comes close
 
 __device__ unsigned int g_gemm_error;
@@ -1038,30 +1038,31 @@ int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, c
   if ((rc = make_map_2d(&tBS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, b_s, N, E * G, N * 4, kBM, gps,
                         CU_TENSOR_MAP_SWIZZLE_NONE, "b_scales")))
     return rc;
-  static bool attr_set = false;  // per template instance
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(w4a8_gemm_kernel<CF, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kMaxDynSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(w4a8_gemm_kernel<CF, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kMaxDynSmem) != cudaSuccess)
-      return check_launch("cudaFuncSetAttribute(gemm)");
-    if constexpr (CF::kRegSplit) {
-      // setmaxnreg.inc waits until the released registers cover the request: the warpgroups'
-      // budgets must fit in what the block is launched with, or the claim would never return.
-      for (int sp = 0; sp < 2; ++sp) {
-        cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, sp ? w4a8_gemm_kernel<CF, true> : w4a8_gemm_kernel<CF, false>) !=
-            cudaSuccess)
-          return check_launch("cudaFuncGetAttributes(gemm)");
-        const int need = 128 * CF::kRegsCtl + 32 * CF::kConvSets * kConvWarps * CF::kRegsConv +
-                         32 * CF::kEpiWarps * CF::kRegsEpi;
-        if (fa.numRegs * CF::kThreads < need)
-          return set_error(W4A8_ERR_UNSUPPORTED, "gemm kernel built with %d registers per thread: %d < %d",
-                           fa.numRegs, fa.numRegs * CF::kThreads, need);
-      }
-    }
-    attr_set = true;
-  }
+  static DeviceOnce attrs;  // per template instance; function attributes are per device
+  if (int rc2 = attrs.run([] {
+        if (cudaFuncSetAttribute(w4a8_gemm_kernel<CF, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kMaxDynSmem) != cudaSuccess ||
+            cudaFuncSetAttribute(w4a8_gemm_kernel<CF, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kMaxDynSmem) != cudaSuccess)
+          return check_launch("cudaFuncSetAttribute(gemm)");
+        if constexpr (CF::kRegSplit) {
+          // setmaxnreg.inc waits until the released registers cover the request: the warpgroups'
+          // budgets must fit in what the block is launched with, or the claim would never return.
+          for (int sp = 0; sp < 2; ++sp) {
+            cudaFuncAttributes fa;
+            if (cudaFuncGetAttributes(&fa, sp ? w4a8_gemm_kernel<CF, true> : w4a8_gemm_kernel<CF, false>) !=
+                cudaSuccess)
+              return check_launch("cudaFuncGetAttributes(gemm)");
+            const int need = 128 * CF::kRegsCtl + 32 * CF::kConvSets * kConvWarps * CF::kRegsConv +
+                             32 * CF::kEpiWarps * CF::kRegsEpi;
+            if (fa.numRegs * CF::kThreads < need)
+              return set_error(W4A8_ERR_UNSUPPORTED, "gemm kernel built with %d registers per thread: %d < %d",
+                               fa.numRegs, fa.numRegs * CF::kThreads, need);
+          }
+        }
+        return static_cast<int>(W4A8_OK);
+      }))
+    return rc2;
   GemmParams p;
   p.seg = seg;
   p.C = C;

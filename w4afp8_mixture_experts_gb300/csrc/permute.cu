@@ -247,15 +247,16 @@ extern "C" int moe_permute_ep(const int32_t* topk_ids, int64_t T, int k, int64_t
                "workspace of %zu bytes (4-byte aligned) required for %lld pairs, got %zu", need, (long long)P,
                ws_bytes);
   const size_t smem = static_cast<size_t>(33 * E_local) * sizeof(int);
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 33 * 1024 * 4) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(permute_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 33 * 1024 * 4) !=
-            cudaSuccess)
-      return check_launch("cudaFuncSetAttribute(permute)");
-    attr_set = true;
-  }
+  static DeviceOnce attrs;  // the shared-memory limit is a per-device function attribute
+  if (int rc = attrs.run([] {
+        if (cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 33 * 1024 * 4) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(permute_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 33 * 1024 * 4) != cudaSuccess)
+          return check_launch("cudaFuncSetAttribute(permute)");
+        return static_cast<int>(W4A8_OK);
+      }))
+    return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int Ei = static_cast<int>(E), EL = static_cast<int>(E_local);
   if (need == 0) {
