@@ -677,8 +677,8 @@ def run_linear(args, cfg, dev, world, rank, peaks, peak_src):
            "steps": Kst, "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x int4 -> f32 (bf16 out)", "data": "synthetic",
            "config": {"workload": workload_desc("linear", cfg), "l2": f"{copies} rotating weight copies"},
-           "tflops": round(tf, 2), "roofline": roof, "gpu_launches": Kst * (2 if need else 1),
-           "split_k": (need // (4 * M * N)) if need else 1, "clocks": clk.summary()}
+           "tflops": round(tf, 2), "roofline": roof, "gpu_launches": Kst * (2 if m.linear_split_k(M, N, K) > 1 else 1),
+           "split_k": m.linear_split_k(M, N, K), "clocks": clk.summary()}
     if rank == 0:
         print(json.dumps(res), flush=True)
 

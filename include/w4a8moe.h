@@ -38,9 +38,12 @@
  * Activation scales: fp32 [K/128][ld], element (row m, group g) at
  * scales[g*ld + m], ld >= M and ld % 4 == 0 (group-major, so a tile of rows of
  * one group is contiguous for TMA).  Activation corrections gcorr: same layout,
- * gcorr[g][m] = -1/2 * scales[g][m] * sum_{k in g} e4m3(q[m][k]); the
- * quantisation calls emit them and the GEMMs consume them (the prepacked
- * weights encode v + 1/2, whose products the correction removes).
+ * gcorr[g][m] = -1/2 * scales[g][m] * S, S = sum_{k in g} e4m3(q[m][k]) summed
+ * exactly, rounded once to fp32 (exact while |S| < 2^15), then one rounded
+ * fp32 product.  The quantisation calls emit them and the GEMMs consume them
+ * (the prepacked weights encode v + 1/2, whose products the correction
+ * removes); a GEMM given a_gcorr = NULL computes them from A itself, in its
+ * workspace, with the same arithmetic (so the result is the same, bit for bit).
  */
 #ifndef W4A8MOE_H
 #define W4A8MOE_H
@@ -52,7 +55,7 @@
 extern "C" {
 #endif
 
-#define W4A8MOE_ABI_VERSION 3
+#define W4A8MOE_ABI_VERSION 4
 
 typedef enum {
   W4A8_OK = 0,
@@ -175,7 +178,12 @@ int fp8_quant_scatter_per_token_group(const uint16_t* x, int64_t T, int64_t K, c
  *   seg_indptr int64 [E+1] (device; seg_indptr[E] must equal M_total)
  *   C bf16 [M_total][N]
  *   K % 128 == 0, N % 128 == 0, 1 <= E <= 1024, M_total < 2^31.
- * Rows outside every segment are not written.  ws may be NULL (none needed).
+ * Rows outside every segment are not written.
+ * a_gcorr may be NULL: the call then first computes the corrections of all
+ * M_total rows from A and a_scales (one extra pass over A) into ws, which must
+ * hold (K/128) * a_scale_ld fp32 (16-byte aligned; w4a8_workspace_bytes(
+ * W4A8_OP_GROUPED_GEMM, M_total, N, K, E) for a_scale_ld = M_total rounded up
+ * to 4).  With a_gcorr given, ws may be NULL (none needed).
  * The kernel configuration follows from the host-known M_total / E (the mean
  * rows per expert) and K: up to 32, 16-row token tiles; from 128, 128-row
  * tiles; in between, two kernel launches over disjoint experts (those with at
@@ -236,12 +244,22 @@ int moe_unpermute_combine(const uint16_t* Y, const int32_t* src2dst, const float
  *   A uint8 [M][K]   a_scales, a_gcorr fp32 [K/128][a_scale_ld]
  *   B_prepacked uint8 [N][K/2]   b_scales fp32 [K/128][N]   C bf16 [M][N]
  *   K % 128 == 0, N % 128 == 0.
- * ws: at least w4a8_workspace_bytes(W4A8_OP_LINEAR, M, N, K, 1) bytes (the
- * split-K partial sums of small-M shapes); may be NULL when that is 0.
+ * ws: w4a8_workspace_bytes(W4A8_OP_LINEAR, M, N, K, 1) bytes, 16-byte
+ * aligned, always suffice for a_scale_ld = M rounded up to 4: the split-K
+ * partial sums of small-M shapes (w4a8_linear_split_k(M, N, K) > 1), then, at
+ * the next 256-byte boundary, the corrections when a_gcorr is NULL (as in
+ * (4)).  With a_gcorr given and no split, ws may be NULL.
  */
 int w4a8_linear(const uint8_t* A, const float* a_scales, const float* a_gcorr, int64_t a_scale_ld,
                 const uint8_t* B_prepacked, const float* b_scales, int64_t M, int64_t N, int64_t K,
                 uint16_t* C, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * K splits (1 = none) w4a8_linear uses for this shape on the current device:
+ * when the 128-row tiles are fewer than the SMs, each tile's K range is cut
+ * into pieces whose fp32 partial sums a second kernel adds.  Diagnostic.
+ */
+int w4a8_linear_split_k(int64_t M, int64_t N, int64_t K);
 
 /* Operation ids for w4a8_workspace_bytes. */
 #define W4A8_OP_PERMUTE 1
@@ -300,7 +318,10 @@ int w4a8_moe_forward_ep(const uint16_t* x, const float* logits, int64_t T, int64
  *   The call itself never calls cudaMalloc / cudaFree or any allocating routine.
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.  All calls share the one array and it keeps the
+ *   before any stream capture.  With CUDA's lazy module loading (the default),
+ *   that first call may also be when the driver places the array in the
+ *   device's memory: a caller whose allocator is to own the rest of the
+ *   device should make it at start-up, before handing memory to that allocator.  All calls share the one array and it keeps the
  *   last call's contents: calls that overlap on the GPU (other streams, other
  *   host threads) race and corrupt each other; order them on one stream.
  */

@@ -50,11 +50,13 @@ def bf16_ulp_diff(a_bits, b_bits):
 
 
 def gcorr_of(aq, a_s):
-    """The activation correction the GEMMs consume: -1/2 * scale * sum of E4M3 values, fp32 [M, G]."""
+    """The activation correction the GEMMs consume: -1/2 * scale * (sum of the group's E4M3 values), fp32 [M, G].
+
+    The sum is exact (float64 holds it), rounded once to fp32, then one fp32 product with the scale."""
     from oracle import e4m3
     M, K = aq.shape
-    S = e4m3.decode(aq).reshape(M, K // 128, 128).sum(axis=2)
-    return (np.float32(-0.5) * (np.asarray(a_s, np.float32) * S.astype(np.float32))).astype(np.float32)
+    S = e4m3.decode(aq).reshape(M, K // 128, 128).sum(axis=2).astype(np.float32)
+    return (np.float32(-0.5) * (np.asarray(a_s, np.float32) * S)).astype(np.float32)
 
 
 def prepacked(lib, packed):

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(clib):
 
 
 def test_status_strings_and_version(clib):
-    assert clib.w4a8_abi_version() == 3
+    assert clib.w4a8_abi_version() == 4
     assert clib.w4a8_status_string(0) == b"ok"
     assert clib.w4a8_status_string(1) == b"invalid argument"
     assert clib.w4a8_status_string(4) == b"device-side wait timed out"
@@ -64,7 +64,11 @@ P16 = ctypes.c_void_p(16)  # a 16-byte aligned non-null dummy (never dereference
     (lambda L: L.w4a8_grouped_gemm(P16, P16, P16, 4, P16, P16, P16, 2, 100, 256, 4, P16, NULL, 0, NULL), b"N=100"),
     (lambda L: L.w4a8_grouped_gemm(P16, P16, P16, 4, P16, P16, NULL, 2, 128, 256, 4, P16, NULL, 0, NULL),
      b"seg_indptr"),
-    (lambda L: L.w4a8_linear(P16, P16, NULL, 4, P16, P16, 4, 128, 256, P16, NULL, 0, NULL), b"null"),
+    (lambda L: L.w4a8_linear(P16, P16, P16, 4, NULL, P16, 4, 128, 256, P16, NULL, 0, NULL), b"null"),
+    # no caller corrections: the call computes them and needs (K/128) x ld fp32 of workspace
+    (lambda L: L.w4a8_linear(P16, P16, NULL, 4, P16, P16, 4, 128, 256, P16, NULL, 0, NULL), b"workspace"),
+    (lambda L: L.w4a8_grouped_gemm(P16, P16, NULL, 4, P16, P16, P16, 2, 128, 256, 4, P16, P16, 16, NULL),
+     b"workspace"),
     (lambda L: L.w4a8_linear(P16, P16, ctypes.c_void_p(20), 4, P16, P16, 4, 128, 256, P16, NULL, 0, NULL),
      b"aligned"),
     (lambda L: L.silu_mul_requant(P16, 4, 100, P16, P16, NULL, 4, NULL), b"I=100"),
@@ -95,3 +99,11 @@ def test_moe_workspace_layout(clib):
     assert L.scale_ld == P and L.total >= P * 7168 + P * 4096 * 2 + P * 2048 + P * 7168 * 2
     assert clib.w4a8_moe_workspace_bytes(64, 7168, 2048, 256, 8) == L.total
     assert clib.w4a8_moe_noalloc_scratch_bytes() == 64 << 20
+
+
+def test_gemm_workspace_sizes(clib):
+    # the corrections of M rows (ld = M rounded up to 4) over K/128 groups, after the split-K partials
+    assert clib.w4a8_workspace_bytes(2, 300, 256, 1024, 8) == 8 * 300 * 4
+    assert clib.w4a8_workspace_bytes(2, 5, 256, 1024, 8) == 8 * 8 * 4
+    assert clib.w4a8_workspace_bytes(3, 1000, 128, 256, 1) == 2 * 1000 * 4  # no split at this shape
+    assert clib.w4a8_workspace_bytes(2, 0, 256, 1024, 8) == 0

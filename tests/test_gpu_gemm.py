@@ -11,7 +11,7 @@ import torch
 import inputs
 import oracle
 from oracle import e4m3
-from gpu_util import f64_of_bf16, gcorr_of, prepacked, rel_fro, scales_to_gpu_layout, to_dev
+from gpu_util import f64_of_bf16, gcorr_of, prepacked, rel_fro, scales_from_gpu_layout, scales_to_gpu_layout, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -114,7 +114,7 @@ def test_linear(lib, M, N, K):
 # fp32 partials (decode tiles for M <= 32, 128-row tiles above).
 @pytest.mark.parametrize("M,N,K", [(1, 1024, 8192), (13, 512, 4096), (40, 256, 16384), (130, 256, 32768)])
 def test_linear_split_k(lib, M, N, K):
-    assert lib.linear_workspace_bytes(M, N, K) > 0
+    assert lib.linear_split_k(M, N, K) > 1
     rng = np.random.default_rng(M * 11 + N + K)
     aq, a_s = _acts(rng, M, K)
     packed, ws = _weights(rng, 1, N, K)
@@ -194,7 +194,57 @@ def test_linear_sweep_shapes(lib, N, K):
     o = 0
     for (M, n), g in zip(spans, got):
         err = rel_fro(g, ref[o:o + n])
-        print(f"Linear M={M} N={N} K={K} (split-K {lib.linear_workspace_bytes(M, N, K) // (4 * M * N) or 1}): "
+        print(f"Linear M={M} N={N} K={K} (split-K {lib.linear_split_k(M, N, K)}): "
               f"{n} rows, rel Frobenius {err:.2e}")
         assert err <= 1e-3, (M, err)
         o += n
+
+
+# a_gcorr = NULL: the GEMM computes the activation corrections from the codes itself (into its
+# workspace), with the quantisation kernels' arithmetic, so the result is the one it gives with the
+# corrections the quantisation emits, bit for bit; and within the stage tolerance of the oracle.
+@pytest.mark.parametrize("kind,M,N,K", [("grouped", 0, 256, 512), ("grouped", 3000, 128, 1024),
+                                        ("linear", 1, 1024, 8192), ("linear", 200, 384, 2048),
+                                        ("linear", 1000, 256, 256)])
+def test_gemm_without_caller_corrections(lib, kind, M, N, K):
+    from gpu_util import bf16_from_bits
+    rng = np.random.default_rng(M + N + K)
+    if kind == "grouped":
+        counts = [40, 0, 7, 300, 1] if M == 0 else list(rng.multinomial(M, [0.5, 0.3, 0.2]))
+        M = int(sum(counts))
+        seg = np.concatenate([[0], np.cumsum(counts)])
+    xb = inputs.to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    aq, a_s, a_c = lib.fp8_quant_per_token_group(bf16_from_bits(xb))
+    E = len(seg) - 1 if kind == "grouped" else 1
+    packed, ws = _weights(rng, E, N, K)
+    if kind == "grouped":
+        B, bs, sg = prepacked(lib, packed), to_dev(ws), to_dev(seg.astype(np.int64))
+        with_c = lib.w4a8_grouped_gemm(aq, a_s, a_c, B, bs, sg)
+        without = lib.w4a8_grouped_gemm(aq, a_s, None, B, bs, sg)
+        ref = _oracle_grouped(aq.cpu().numpy(), scales_from_gpu_layout(a_s, M), packed, ws, seg)
+    else:
+        B, bs = prepacked(lib, packed[0]), to_dev(ws[0])
+        with_c = lib.w4a8_linear(aq, a_s, a_c, B, bs)
+        without = lib.w4a8_linear(aq, a_s, None, B, bs)
+        ref = oracle.linear(aq.cpu().numpy(), scales_from_gpu_layout(a_s, M), oracle.unpack_int4(packed[0]), ws[0].T)
+    assert lib.device_error() == 0
+    assert torch.equal(with_c, without)
+    assert rel_fro(f64_of_bf16(without), ref) <= 1e-3
+
+
+def test_gemm_without_corrections_needs_workspace(lib):
+    rng = np.random.default_rng(3)
+    M, N, K = 64, 128, 256
+    aq, a_s = _acts(rng, M, K)
+    packed, ws = _weights(rng, 1, N, K)
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    rc = lib.load().w4a8_linear(to_dev(aq).data_ptr(), scales_to_gpu_layout(a_s).data_ptr(), None,
+                                scale_ld_of(M), prepacked(lib, packed[0]).data_ptr(), to_dev(ws[0]).data_ptr(),
+                                M, N, K, C.data_ptr(), small.data_ptr(), small.numel(), None)
+    assert rc == 1  # W4A8_ERR_INVALID_ARG: the corrections need (K/128) x ld fp32 of workspace
+    assert lib.linear_workspace_bytes(M, N, K) >= (K // 128) * scale_ld_of(M) * 4
+
+
+def scale_ld_of(M):
+    return max(4, (M + 3) // 4 * 4)

@@ -106,12 +106,31 @@ def test_quant(lib, M, K):
 
 
 def _check_gcorr(gc, codes, scales):
-    # -1/2 * scale * (sum of the group's E4M3 values): the sum is exact in float64
+    # -1/2 * scale * S with S the exact sum of the group's E4M3 values, rounded once to fp32, then one
+    # fp32 product: bit for bit
     M, K = codes.shape
     S = oracle.e4m3.decode(codes).reshape(M, K // 128, 128).sum(axis=2)
-    ref = -0.5 * scales.astype(np.float64) * S
-    tol = 1e-6 * (0.5 * scales.astype(np.float64) * np.abs(oracle.e4m3.decode(codes)).reshape(M, K // 128, 128).sum(2))
-    assert np.all(np.abs(gc - ref) <= tol + 1e-30)
+    ref = (np.float32(-0.5) * (scales.astype(np.float32) * S.astype(np.float32))).astype(np.float32)
+    assert np.array_equal(gc, ref)
+
+
+def test_gcorr_sum_is_exact_past_the_fp32_grid(lib):
+    # Groups whose code sum passes 2^15 while holding values on the 2^-9 grid: a running fp32 sum would
+    # round there, the exact sum must not (the correction is rounded once, at the end).
+    K = 256
+    x = np.zeros((4, K), np.float32)
+    x[:, :100] = 1.0                                  # codes 448 (0x7E)
+    x[:, 100:128] = np.float32(1.0 / 448 * 0.40625)  # tiny codes with fine bits
+    x[1, 128:] = -1.0
+    x[2, :128] *= -1
+    x[3, 1:128:2] = np.float32(3.0 / 448 * 0.0078125)
+    xb = inputs.to_bf16_bits(x)
+    q, s, c = lib.fp8_quant_per_token_group(bf16_from_bits(xb))
+    rq, rs = oracle.quant_per_token_group(inputs.bf16_bits_to_f32(xb))
+    assert np.array_equal(q.cpu().numpy(), rq)
+    S = oracle.e4m3.decode(rq).reshape(4, 2, 128).sum(axis=2)
+    assert np.abs(S).max() > 2 ** 15
+    _check_gcorr(scales_from_gpu_layout(c, 4), rq, rs)
 
 
 def test_quant_gather(lib):

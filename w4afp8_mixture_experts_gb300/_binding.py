@@ -41,6 +41,7 @@ _SIGS = {
     "w4a8_linear": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp,
                              _c_sz, _c_vp]),
     "w4a8_workspace_bytes": (_c_sz, [_c_int, _c_i64, _c_i64, _c_i64, _c_i64]),
+    "w4a8_linear_split_k": (_c_int, [_c_i64, _c_i64, _c_i64]),
     "w4a8_moe_forward": (_c_int, [_c_vp, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_vp,
                                   _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]),
     "w4a8_moe_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_i64, _c_i64, _c_int]),
@@ -202,21 +203,26 @@ def w4a8_prepack_weights(w):
 
 
 def w4a8_grouped_gemm(A, a_scales, a_gcorr, B_prepacked, b_scales, seg_indptr):
-    """A uint8 [M, K], a_scales / a_gcorr [K/128, ld], B prepacked uint8 [E, N, K/2],
-    b_scales [E, K/128, N] -> bf16 [M, N]."""
+    """A uint8 [M, K], a_scales [K/128, ld], a_gcorr [K/128, ld] or None (the library then computes the
+    corrections from A in a workspace), B prepacked uint8 [E, N, K/2], b_scales [E, K/128, N] -> bf16 [M, N]."""
     _req(A, torch.uint8, "A", 2)
     _req(a_scales, torch.float32, "a_scales", 2)
-    _req(a_gcorr, torch.float32, "a_gcorr", 2)
+    if a_gcorr is not None:
+        _req(a_gcorr, torch.float32, "a_gcorr", 2)
     _req(B_prepacked, torch.uint8, "B_prepacked", 3)
     _req(b_scales, torch.float32, "b_scales", 3)
     _req(seg_indptr, torch.int64, "seg_indptr", 1)
     M, K = A.shape
     E, N, Kh = B_prepacked.shape
-    if Kh * 2 != K or seg_indptr.numel() != E + 1 or a_gcorr.shape != a_scales.shape:
+    if Kh * 2 != K or seg_indptr.numel() != E + 1 or (a_gcorr is not None and a_gcorr.shape != a_scales.shape):
         raise ValueError("shape mismatch")
+    ws = None
+    if a_gcorr is None:  # room for the corrections at this call's scale leading dimension
+        ws = torch.empty((K // 128) * a_scales.shape[1] * 4, dtype=torch.uint8, device=A.device)
     C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     _check(load().w4a8_grouped_gemm(_p(A), _p(a_scales), _p(a_gcorr), a_scales.shape[1], _p(B_prepacked),
-                                    _p(b_scales), _p(seg_indptr), E, N, K, M, _p(C), None, 0, _stream()))
+                                    _p(b_scales), _p(seg_indptr), E, N, K, M, _p(C), _p(ws),
+                                    0 if ws is None else ws.numel(), _stream()))
     return C
 
 
@@ -244,22 +250,31 @@ def moe_unpermute_combine(Y, src2dst, topk_w):
 
 
 def linear_workspace_bytes(M: int, N: int, K: int) -> int:
+    """Workspace of w4a8_linear (split-K partial sums, and room for the corrections when a_gcorr is None)."""
     return int(load().w4a8_workspace_bytes(3, M, N, K, 1))
 
 
+def linear_split_k(M: int, N: int, K: int) -> int:
+    """K splits w4a8_linear uses for this shape on the current device (1: none)."""
+    return int(load().w4a8_linear_split_k(M, N, K))
+
+
 def w4a8_linear(A, a_scales, a_gcorr, B_prepacked, b_scales, ws=None):
-    """A uint8 [M, K], a_scales / a_gcorr [K/128, ld], B prepacked uint8 [N, K/2], b_scales [K/128, N]
-    -> bf16 [M, N]."""
+    """A uint8 [M, K], a_scales [K/128, ld], a_gcorr [K/128, ld] or None (computed by the library),
+    B prepacked uint8 [N, K/2], b_scales [K/128, N] -> bf16 [M, N]."""
     _req(A, torch.uint8, "A", 2)
     _req(a_scales, torch.float32, "a_scales", 2)
-    _req(a_gcorr, torch.float32, "a_gcorr", 2)
+    if a_gcorr is not None:
+        _req(a_gcorr, torch.float32, "a_gcorr", 2)
     _req(B_prepacked, torch.uint8, "B_prepacked", 2)
     _req(b_scales, torch.float32, "b_scales", 2)
     M, K = A.shape
     N = B_prepacked.shape[0]
-    need = linear_workspace_bytes(M, N, K)
-    if need and ws is None:
-        ws = torch.empty(need, dtype=torch.uint8, device=A.device)
+    if ws is None:
+        need = linear_workspace_bytes(M, N, K)
+        if a_gcorr is None:  # the corrections at this call's scale leading dimension
+            need += (K // 128) * (a_scales.shape[1] - scale_ld(M)) * 4
+        ws = torch.empty(need, dtype=torch.uint8, device=A.device) if need else None
     C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     _check(load().w4a8_linear(_p(A), _p(a_scales), _p(a_gcorr), a_scales.shape[1], _p(B_prepacked), _p(b_scales),
                               M, N, K, _p(C), _p(ws), 0 if ws is None else ws.numel(), _stream()))

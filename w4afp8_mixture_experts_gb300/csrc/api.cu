@@ -109,8 +109,8 @@ extern "C" int w4a8_device_error(void) {
 }
 
 extern "C" size_t w4a8_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int64_t E) {
-  (void)E;
-  if (op == W4A8_OP_LINEAR) return w4a8::linear_workspace_bytes(M, N, K);
+  if (op == W4A8_OP_LINEAR) return w4a8::gemm_workspace_bytes(M, N, K, true);
+  if (op == W4A8_OP_GROUPED_GEMM) return w4a8::gemm_workspace_bytes(M, N, K, false);
   if (op == W4A8_OP_PERMUTE) return w4a8::permute_ws_bytes(M, E);
   return 0;
 }

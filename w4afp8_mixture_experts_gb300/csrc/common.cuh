@@ -71,6 +71,12 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int num_sms();
 // split-K partial-sum bytes w4a8_linear needs for this shape on the current device (0: none)
 size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
+// workspace of a GEMM call that also computes the activation corrections itself (a_gcorr NULL, scale
+// leading dimension M rounded up to 4): the split-K partial sums (dense only), then the corrections
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, bool dense);
+// gcorr[g][m] of the E4M3 codes A [M][K] and their scales (the arithmetic of the quantisation kernels)
+int launch_gcorr(const uint8_t* A, int64_t M, int64_t K, const float* a_s, int64_t ld, float* gcorr,
+                 cudaStream_t st);
 // per-chunk expert-count table moe_permute needs for P pairs (0: none)
 size_t permute_ws_bytes(int64_t P, int64_t E);
 
@@ -351,6 +357,16 @@ __device__ __forceinline__ void tmem_ld16x256b_x8(uint32_t taddr, uint32_t* r) {
         "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+// 16 lanes x 32 columns (16x256b shape, 4 repetitions): the first 16 registers of the x8 layout above.
+__device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
 

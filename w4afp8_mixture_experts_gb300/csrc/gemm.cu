@@ -1138,21 +1138,26 @@ int gemm_common(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_
   W4A8_REQUIRE(E * N < (1ll << 31) && K < (1ll << 31), "E*N or K too large");
   W4A8_REQUIRE(a_ld >= M && a_ld % 4 == 0 && a_ld > 0, "a_scale_ld=%lld must be >= M and a multiple of 4",
                (long long)a_ld);
-  W4A8_REQUIRE(A && a_s && a_c && B && b_s && C, "null pointer");
+  W4A8_REQUIRE(A && a_s && B && b_s && C, "null pointer");
   W4A8_REQUIRE(aligned16(A) && aligned16(a_s) && aligned16(a_c) && aligned16(B) && aligned16(b_s) && aligned16(C),
                "device pointers must be 16-byte aligned");
   if (M == 0) return W4A8_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // split-K only for the dense GEMM: the grouped GEMM's tile count depends on device-side seg_indptr
   const int S = seg ? 1 : linear_splits(M, N, K);
-  float* partial = nullptr;
-  if (S > 1) {
-    const size_t need = static_cast<size_t>(S) * M * N * sizeof(float);
-    W4A8_REQUIRE(ws != nullptr && ws_bytes >= need && aligned16(ws),
-                 "workspace of %zu bytes (16-byte aligned) required for this shape, got %zu", need, ws_bytes);
-    partial = static_cast<float*>(ws);
-  }
+  // workspace: [split-K partial sums][corrections, when the caller passes none]
+  const size_t part_bytes = S > 1 ? static_cast<size_t>(S) * M * N * sizeof(float) : 0;
+  const size_t corr_off = (part_bytes + 255) & ~size_t(255);
+  const size_t need = a_c ? part_bytes : corr_off + static_cast<size_t>(K / kGroup) * a_ld * sizeof(float);
+  W4A8_REQUIRE(need == 0 || (ws != nullptr && ws_bytes >= need && aligned16(ws)),
+               "workspace of %zu bytes (16-byte aligned) required for this call, got %zu", need, ws_bytes);
+  float* partial = S > 1 ? static_cast<float*>(ws) : nullptr;
   int rc;
+  if (!a_c) {  // the activation corrections from the codes, as the quantisation kernels compute them
+    float* corr = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + corr_off);
+    if ((rc = launch_gcorr(A, M, K, a_s, a_ld, corr, st))) return rc;
+    a_c = corr;
+  }
   // Few rows per expert: weight streaming, 16-wide token tiles and a deep ring.
   if (M <= 32 * E && seg && K >= 4096)
     rc = launch<CfgDecodeLongK>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st);
@@ -1186,6 +1191,13 @@ size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   return S > 1 ? static_cast<size_t>(S) * M * N * sizeof(float) : 0;
 }
 
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, bool dense) {
+  if (M <= 0 || K <= 0 || K % kGroup) return 0;
+  const size_t part = dense ? linear_workspace_bytes(M, N, K) : 0;
+  const int64_t ld = (M + 3) / 4 * 4;
+  return ((part + 255) & ~size_t(255)) + static_cast<size_t>(K / kGroup) * ld * sizeof(float);
+}
+
 }  // namespace w4a8
 
 extern "C" int w4a8_grouped_gemm(const uint8_t* A, const float* a_scales, const float* a_gcorr, int64_t a_scale_ld,
@@ -1203,6 +1215,8 @@ extern "C" int w4a8_linear(const uint8_t* A, const float* a_scales, const float*
   return w4a8::gemm_common(A, a_scales, a_gcorr, a_scale_ld, B_prepacked, b_scales, nullptr, 1, N, K, M, C, ws,
                            ws_bytes, stream);
 }
+
+extern "C" int w4a8_linear_split_k(int64_t M, int64_t N, int64_t K) { return w4a8::linear_splits(M, N, K); }
 
 extern "C" int w4a8_prepack_weights(const uint8_t* w, int64_t rows, int64_t K, uint8_t* out, void* stream) {
   using namespace w4a8;

@@ -12,7 +12,10 @@
 // GPU that loads this library holds it until the process exits.  Host code can
 // not use the variable's name as a device address, so the first call on each
 // device looks the address up with cudaGetSymbolAddress while that device is
-// current, and later calls reuse it.
+// current, and later calls reuse it.  Under CUDA's lazy module loading that
+// lookup can be the moment the driver loads this file's module and places the
+// array in the device's memory, so a caller that must not see any allocation
+// later makes its first call at start-up.
 #include <mutex>
 
 #include "common.cuh"

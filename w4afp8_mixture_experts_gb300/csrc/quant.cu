@@ -45,6 +45,32 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // always takes 16 (0.143 vs 0.175 ms at 8192 tokens: each group's codes go to k rows).
 constexpr int kSmallLaunchGroups = 1 << 16;
 
+// One lane's share of a group's code sum, in units of 2^-9: every E4M3 value is a multiple of 2^-9
+// and at most 448 (229376 units), so the fp32 partial sum of a lane's at most 32 values stays on the
+// 2^-9 grid below 2^15 (24 significant bits) and it and its conversion to units are exact.
+template <int NW>
+__device__ __forceinline__ int code_units(const uint32_t (&code)[NW]) {
+  float sum = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NW; ++i)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      // E4M3 pairs -> f16 pairs (exact) -> fp32
+      uint32_t h2;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(code[i] >> (16 * h))));
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+      sum += f.x + f.y;
+    }
+  return __float2int_rn(sum * 512.0f);
+}
+
+// The group correction -1/2 * s * S from the exact code sum of the whole group, U units of 2^-9
+// (|U| < 2^25, an int32): S = U * 2^-9 is rounded to fp32 once (exact while |S| < 2^15), then one
+// rounded fp32 product with s; the halving is exact.
+__device__ __forceinline__ float corr_from_units(int units, float s) {
+  return -0.5f * __fmul_rn(s, __int2float_rn(units) * (1.0f / 512.0f));
+}
+
 // One (row, 128-group) quantised by its LANES lanes, lane `sub` holding values [sub*V, sub*V + V)
 // (V = 128 / LANES) of the group at xg: the codes (4 per word) stay in registers, with the scale s
 // and the group correction -1/2 * s * sum(E4M3 values) (when want_corr) returned to every lane.
@@ -72,7 +98,6 @@ __device__ __forceinline__ void quantize_group(const uint16_t* __restrict__ xg, 
   const float amax = fmaxf(__uint_as_float(mx << 16), 1e-12f);
   s = __fdiv_rn(amax, 448.0f);
   const float r = __frcp_rn(s);
-  float sum = 0.0f;
 #pragma unroll
   for (int i = 0; i < kQuantVals / 8; ++i) {
     uint32_t c[4];
@@ -81,24 +106,16 @@ __device__ __forceinline__ void quantize_group(const uint16_t* __restrict__ xg, 
       const uint32_t v = w[4 * i + j];
       c[j] = e4m3x2(div_by_scale(bf16_lo(v), s, r), div_by_scale(bf16_hi(v), s, r));
     }
-    if (want_corr) {
-      // E4M3 pairs -> f16 pairs (exact) -> fp32 partial sums
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t h2;
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(c[j])));
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-        sum += f.x + f.y;
-      }
-    }
     code[2 * i] = c[0] | (c[1] << 16);
     code[2 * i + 1] = c[2] | (c[3] << 16);
   }
+  corr = 0.0f;
   if (want_corr) {
+    int u = code_units(code);
 #pragma unroll
-    for (int o = 1; o < LANES; o <<= 1) sum += __shfl_xor_sync(quad, sum, o);
+    for (int o = 1; o < LANES; o <<= 1) u += __shfl_xor_sync(quad, u, o);
+    corr = corr_from_units(u, s);
   }
-  corr = -0.5f * __fmul_rn(s, sum);
 }
 
 // The lane's codes of one group to q (16-byte stores when a lane holds a multiple of 16 codes).
@@ -230,35 +247,66 @@ __global__ void __launch_bounds__(256)
   const float s = __fdiv_rn(amax, 448.0f);
   const float r = __frcp_rn(s);
   uint8_t* qp = q + row * I + g * kGroup + sub * kQuantVals;
-  float sum = 0.0f;
+  uint32_t code[kQuantVals / 4];
 #pragma unroll
   for (int i = 0; i < kQuantVals / 8; ++i) {
     uint32_t c[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
       c[j] = e4m3x2(div_by_scale(h[8 * i + 2 * j], s, r), div_by_scale(h[8 * i + 2 * j + 1], s, r));
-    if (gcorr) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t h2;
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(c[j])));
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-        sum += f.x + f.y;
-      }
-    }
-    reinterpret_cast<uint2*>(qp)[i] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+    code[2 * i] = c[0] | (c[1] << 16);
+    code[2 * i + 1] = c[2] | (c[3] << 16);
+    reinterpret_cast<uint2*>(qp)[i] = make_uint2(code[2 * i], code[2 * i + 1]);
   }
+  float corr = 0.0f;
   if (gcorr) {
+    int u = code_units(code);
 #pragma unroll
-    for (int o = 1; o < LANES; o <<= 1) sum += __shfl_xor_sync(quad, sum, o);
+    for (int o = 1; o < LANES; o <<= 1) u += __shfl_xor_sync(quad, u, o);
+    corr = corr_from_units(u, s);
   }
   if (sub == 0) {
     scales[g * ld + row] = s;
-    if (gcorr) gcorr[g * ld + row] = -0.5f * __fmul_rn(s, sum);
+    if (gcorr) gcorr[g * ld + row] = corr;
   }
 }
 
+// The corrections of stored codes: gcorr[g][m] = -1/2 * a_s[g][m] * (sum of the E4M3 values of A[m]'s
+// group g), 16 lanes per (row, group), with the arithmetic of the quantisation kernels above (so the
+// result equals what they emit for the same codes, bit for bit).  Tasks run group-major, so
+// consecutive groups of 16 lanes write consecutive entries of one gcorr row.
+__global__ void __launch_bounds__(256) gcorr_kernel(const uint8_t* __restrict__ A, int64_t M, int64_t K,
+                                                    const float* __restrict__ a_s, int64_t ld,
+                                                    float* __restrict__ gcorr) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t G = K / kGroup;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t task = tid / 16;
+  const int sub = static_cast<int>(tid % 16);
+  if (task >= M * G) return;  // a group's lanes leave together
+  const int64_t g = task / M;
+  const int64_t m = task - g * M;
+  const uint2 v = __ldg(reinterpret_cast<const uint2*>(A + m * K + g * kGroup + sub * 8));
+  const uint32_t code[2] = {v.x, v.y};
+  int u = code_units(code);
+  const unsigned half = 0xFFFFu << (threadIdx.x & 16);
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) u += __shfl_xor_sync(half, u, o);
+  if (sub == 0) gcorr[g * ld + m] = corr_from_units(u, a_s[g * ld + m]);
+}
+
 }  // namespace
+
+int launch_gcorr(const uint8_t* A, int64_t M, int64_t K, const float* a_s, int64_t ld, float* gcorr,
+                 cudaStream_t st) {
+  const int64_t blocks = ceil_div(M * (K / kGroup) * 16, 256);
+  W4A8_REQUIRE(blocks < (1ll << 31), "too many rows");
+  if (M == 0) return W4A8_OK;
+  return launch_pdl("gcorr_kernel", gcorr_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, A, M, K,
+                    a_s, ld, gcorr);
+}
+
 }  // namespace w4a8
 
 extern "C" int fp8_quant_per_token_group(const uint16_t* x, int64_t M_src, int64_t K, const int32_t* row_index,
