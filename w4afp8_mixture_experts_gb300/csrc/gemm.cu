@@ -156,13 +156,17 @@ struct Cfg {
   static constexpr int kMmaCommits = kMmaByStage ? 1 : MMAS_;
   static_assert(!kMmaByStage || (TSTAGES_ % MMAS_ == 0 && ABUF_ % MMAS_ == 0),
                 "stage-wise MMA warps: token and A ring depths must be multiples of the MMA warps");
-  static constexpr int kRegsCtl = 72;    // warps 0-3: the two producers and the MMA warps
-  static constexpr int kRegsConv = 96;   // converter warpgroups
-  static constexpr int kRegsEpi = 168;   // epilogue warpgroups
-  static_assert(!kRegSplit || (kThreads == 512 && kWarpConv0 == 4 && kWarpEpi0 % 4 == 0),
-                "register split: warp roles aligned to warpgroups, 512 threads");
+  // Registers a thread gets at launch (the block's share of the 64 K register file, in steps of 8), and the
+  // per-warpgroup budgets.  With two converter sets (640 threads) the converters work on quarter rows and
+  // fit in 40 registers.
+  static constexpr int kLaunchRegs = (65536 / kThreads) / 8 * 8 > 255 ? 255 : (65536 / kThreads) / 8 * 8;
+  static constexpr int kRegsCtl = SETS_ > 1 ? 48 : 72;   // warps 0-3: the two producers and the MMA warps
+  static constexpr int kRegsConv = SETS_ > 1 ? 48 : 96;  // converter warpgroups
+  static constexpr int kRegsEpi = 168;                   // epilogue warpgroups
+  static_assert(!kRegSplit || (kWarpConv0 == 4 && kWarpEpi0 % 4 == 0 && kEpiWarps % 4 == 0),
+                "register split: warp roles aligned to warpgroups");
   static_assert(!kRegSplit || 128 * kRegsCtl + 32 * kConvSets * kConvWarps * kRegsConv + 32 * EPIW_ * kRegsEpi <=
-                                  kThreads * 128,
+                                  kThreads * kLaunchRegs,
                 "register split exceeds the registers the block is launched with");
 };
 
@@ -631,6 +635,20 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
               tmem_st16(tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) + CF::kAColBase + (a * GPS + j) * 32 + 16 * hh,
                         out);
             }
+          } else if constexpr (kConvSets > 1) {
+            // quarter rows (16 packed bytes -> 32 E4M3 bytes at a time): few registers, several sets
+            uint8_t* arow = s_a + (a * GPS + j) * CF::kABytes + r * 128;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((q ^ ((r >> 1) & 3)) << 4));
+              const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+              uint32_t out[8];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) int4x8_to_e4m3x8(in[i], out[2 * i], out[2 * i + 1]);
+              *reinterpret_cast<uint4*>(arow + (((2 * q) ^ (r & 7)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+              *reinterpret_cast<uint4*>(arow + (((2 * q + 1) ^ (r & 7)) << 4)) =
+                  make_uint4(out[4], out[5], out[6], out[7]);
+            }
           } else {
             uint32_t in[16];
 #pragma unroll
@@ -715,28 +733,44 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
               if (c0 + 64 * b >= need) continue;  // warp-uniform
-              uint32_t p[64];
-              const uint32_t pa = tmem_base + t_lane + (pslot * GPS + j) * NMAX + c0 + 64 * b;
-              tmem_ld16x256b_x8(pa, p);                    // lanes q4*32 + 0 .. 15
-              tmem_ld16x256b_x8(pa + (16u << 16), p + 32);  // lanes q4*32 + 16 .. 31
-              uint64_t ws2[4];
+              // this group's scales first: their shared-memory latency overlaps the partial reads
+              uint64_t ws2[4], t2[8], k2[8];
 #pragma unroll
               for (int rho = 0; rho < 4; ++rho) {
                 const float w = wsj[8 * rho];
                 asm("mov.b64 %0, {%1, %1};" : "=l"(ws2[rho]) : "f"(w));
               }
-              tmem_wait_ld_pin<64>(p);
 #pragma unroll
               for (int v = 0; v < 8; ++v) {
-                const uint64_t t2 = *reinterpret_cast<const uint64_t*>(ts + 64 * b + 8 * v);
-                const uint64_t k2 = *reinterpret_cast<const uint64_t*>(tc + 64 * b + 8 * v);
+                t2[v] = *reinterpret_cast<const uint64_t*>(ts + 64 * b + 8 * v);
+                k2[v] = *reinterpret_cast<const uint64_t*>(tc + 64 * b + 8 * v);
+              }
+              // the partials in four 16-column chunks, the read of chunk c + 1 in flight while chunk c
+              // is promoted
+              const uint32_t pa = tmem_base + t_lane + (pslot * GPS + j) * NMAX + c0 + 64 * b;
+              uint32_t q0[16], q1[16];
+              tmem_ld16x256b_x2(pa, q0);
+              tmem_ld16x256b_x2(pa + (16u << 16), q0 + 8);
+              tmem_wait_ld_pin<16>(q0);
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
+              for (int c = 0; c < 4; ++c) {
+                uint32_t* cur = (c & 1) ? q1 : q0;
+                uint32_t* nxt = (c & 1) ? q0 : q1;
+                if (c < 3) {
+                  tmem_ld16x256b_x2(pa + 16 * (c + 1), nxt);
+                  tmem_ld16x256b_x2(pa + 16 * (c + 1) + (16u << 16), nxt + 8);
+                }
 #pragma unroll
-                  for (int jj = 0; jj < 2; ++jj) {
-                    const int i = 32 * h + 4 * v + 2 * jj;
-                    promote2p(acc2[b][2 * h + jj][v], ws2[2 * h + jj], t2, k2, p[i], p[i + 1]);
-                  }
+                for (int vl = 0; vl < 2; ++vl)
+#pragma unroll
+                  for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                      const int i = 8 * h + 4 * vl + 2 * jj;
+                      promote2p(acc2[b][2 * h + jj][2 * c + vl], ws2[2 * h + jj], t2[2 * c + vl], k2[2 * c + vl],
+                                cur[i], cur[i + 1]);
+                    }
+                if (c < 3) tmem_wait_ld_pin<16>(nxt);
               }
             }
           }
@@ -1098,7 +1132,7 @@ using CfgDecodeLongK = Cfg<16, 4, 5, 4, 6, 2, 3, true, 2, 4, 4, 1>;
 // paid once per two groups), so the fp32 partials of 2 slots x 2 groups fill the tensor memory and the
 // converted weights go to shared memory (prefill w13 4.378 -> 4.320 ms, w2 2.589 -> 2.504 ms against
 // one group per stage with the weights in tensor memory)
-using CfgPrefill = Cfg<128, 2, 4, 2, 4, 2, 2, false, 1, 2, 8, 1>;
+using CfgPrefill = Cfg<128, 2, 4, 2, 4, 2, 2, false, 2, 2, 8, 1>;
 
 // C[m][n] = bf16(sum over s of partial[s][m][n]), four columns per thread.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ partial,
