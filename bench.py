@@ -303,11 +303,18 @@ def linear_counts(M, N, K):
     return {"flops": 2.0 * M * N * K, "bytes": N * K // 2 + N * G * 4 + M * K + M * G * 4 + M * N * 2}
 
 
-def moe_launches_per_step(n_stages, two_pass_permute, pairs, experts):
+def moe_launches_per_step(n_stages, two_pass_permute, gemm_plans):
     """Kernels one layer step launches: one per stage, plus the permutation's count pass from 8192 pairs,
-    plus a second launch of each grouped GEMM when the mean rows per expert lie strictly between 32 and
-    128 (experts with at most 16 rows on the narrow tiles, the rest on the wide ones)."""
-    return n_stages + (1 if two_pass_permute else 0) + (2 if 32 * experts < pairs < 128 * experts else 0)
+    plus a second launch for each grouped GEMM whose plan (w4a8_grouped_gemm_plan: 1 narrow tiles, 2 wide
+    tiles, 3 both over disjoint experts) is the split one."""
+    return n_stages + (1 if two_pass_permute else 0) + sum(1 for p in gemm_plans if p == 3)
+
+
+def gemm_plans(lib, pairs, experts, H, I):
+    """The launch plans of the layer's w13 (K = H) and w2 (K = I) grouped GEMMs."""
+    import ctypes
+    th = ctypes.c_int()
+    return [int(lib.w4a8_grouped_gemm_plan(pairs, experts, K, ctypes.byref(th))) for K in (H, I)]
 
 
 def roofline_core(alg_bytes, flops, ms, hbm_gbs, tensor_tflops):
@@ -596,7 +603,7 @@ def measure_moe(r, name, cfg, args, dev, world, peaks, peak_src):
         "stages_note": "stage breakdown from a separate pass with an event after every stage; the timed "
                        "region runs the stages back to back with events only around w13",
         "roofline": roof,
-        "gpu_launches": moe_launches_per_step(nst, r.permute_ws_bytes > 0, T * k, r.EL) * K,
+        "gpu_launches": moe_launches_per_step(nst, r.permute_ws_bytes > 0, gemm_plans(r.lib, T * k, r.EL, H, I)) * K,
         "clocks": clk.summary(),
     }
 

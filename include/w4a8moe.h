@@ -184,11 +184,11 @@ int fp8_quant_scatter_per_token_group(const uint16_t* x, int64_t T, int64_t K, c
  * hold (K/128) * a_scale_ld fp32 (16-byte aligned; w4a8_workspace_bytes(
  * W4A8_OP_GROUPED_GEMM, M_total, N, K, E) for a_scale_ld = M_total rounded up
  * to 4).  With a_gcorr given, ws may be NULL (none needed).
- * The kernel configuration follows from the host-known M_total / E (the mean
- * rows per expert) and K: up to 32, 16-row token tiles; from 128, 128-row
- * tiles; in between, two kernel launches over disjoint experts (those with at
- * most 16 rows on 16-row tiles, the others on 128-row tiles).  Every
- * configuration computes each output element with the same fp32 operations.
+ * The kernel configuration follows w4a8_grouped_gemm_plan(M_total, E, K):
+ * 16-row token tiles, 128-row tiles, or two launches over disjoint experts
+ * (those with at most theta rows, counted on the device, on 16-row tiles).
+ * Every configuration computes each output element with the same fp32
+ * operations.
  */
 int w4a8_grouped_gemm(const uint8_t* A, const float* a_scales, const float* a_gcorr,
                       int64_t a_scale_ld, const uint8_t* B_prepacked, const float* b_scales,
@@ -260,6 +260,26 @@ int w4a8_linear(const uint8_t* A, const float* a_scales, const float* a_gcorr, i
  * into pieces whose fp32 partial sums a second kernel adds.  Diagnostic.
  */
 int w4a8_linear_split_k(int64_t M, int64_t N, int64_t K);
+
+/*
+ * Launch plan of (4) for M_total rows over E experts at this K: 1 = 16-row
+ * token tiles, 2 = 128-row tiles, 3 = both, experts with at most *theta rows
+ * (written when theta is not NULL) on the 16-row tiles.  The choice is the
+ * expected-cost argmin of the DeepGEMM PR #53 page's tile cost model
+ * (Conversation, the cost-model commit: cost = a * R + b * T over the tiles T
+ * and the rows R they pad to, in expectation over Poisson row counts),
+ * restated for these tiles: in units of one 16-row tile, cost_16(x) =
+ * ceil(x / 16), cost_128(x) = 2 * tiles + 0.004 * (rows padded to 16 per tile)
+ * (w4a8_tile_cost), theta the largest x with cost_16 <= cost_128 (32), the
+ * split plan paying one launch start-up; and the split is kept whenever
+ * theta * E < M_total < 128 * E, where skewed routing puts experts on both
+ * sides of theta.  0 for an empty or invalid shape.  Host only, no GPU needed.
+ */
+int w4a8_grouped_gemm_plan(int64_t M_total, int64_t E, int64_t K, int* theta);
+/* cost_16 (wide = 0) or cost_128 (wide = 1) of one expert with `rows` rows per
+ * 128-row weight block, and its expectation over Poisson(mean_rows) rows. */
+double w4a8_tile_cost(int wide, int64_t rows);
+double w4a8_expected_tile_cost(int wide, double mean_rows);
 
 /* Operation ids for w4a8_workspace_bytes. */
 #define W4A8_OP_PERMUTE 1

@@ -102,16 +102,11 @@ def test_roofline_core_picks_the_larger_bound():
 
 
 def test_launch_counts():
-    # decode: 512 pairs over 256 experts (2 rows per expert), one-pass permutation
-    assert bench.moe_launches_per_step(7, False, 512, 256) == 7
-    # prefill: 65536 pairs, 256 rows per expert: two-pass permutation, one launch per grouped GEMM
-    assert bench.moe_launches_per_step(7, True, 65536, 256) == 8
-    # skewed: 32768 pairs over 384 experts (85 rows per expert): both grouped GEMMs split by expert size
-    assert bench.moe_launches_per_step(7, True, 32768, 384) == 10
-    # the split is strict at both ends
-    assert bench.moe_launches_per_step(7, False, 32 * 8, 8) == 7
-    assert bench.moe_launches_per_step(7, False, 128 * 8, 8) == 7
-    assert bench.moe_launches_per_step(7, False, 32 * 8 + 1, 8) == 9
+    # seven stages; the permutation's count pass from 8192 pairs; one more launch per split GEMM plan
+    assert bench.moe_launches_per_step(7, False, [1, 1]) == 7
+    assert bench.moe_launches_per_step(7, True, [2, 2]) == 8
+    assert bench.moe_launches_per_step(7, True, [3, 3]) == 10
+    assert bench.moe_launches_per_step(7, False, [3, 2]) == 8
 
 
 def test_throughput_is_whole_job():

@@ -78,9 +78,10 @@ def test_every_int4_value(lib, M):
     ([0, 0, 0, 500], 128, 128),
     ([2, 0, 5, 1, 31, 3], 256, 4096),                # long K: the small-M pipeline with 4 MMA warps
     ([7, 1, 0, 16, 9], 128, 7168),
-    ([500, 3, 0, 15, 16, 17, 40, 1], 256, 512),      # 32 to 128 rows per expert: experts <= 16 rows in their own launch
+    ([500, 3, 0, 15, 16, 17, 40, 1], 256, 512),      # 32 to 128 rows per expert: experts <= 32 rows in their own launch
     ([300, 1, 16, 0, 2], 128, 4096),
     ([2000, 3, 0, 15], 128, 256),                    # >= 128 rows per expert: one launch, 128-wide tiles for all
+    ([33, 32, 31, 0, 64, 20], 128, 1024),            # mean 30 rows: one side of the 32-row crossover or the other
 ])
 def test_grouped_gemm(lib, counts, N, K):
     rng = np.random.default_rng(sum(counts) + N + K)

@@ -155,21 +155,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// As mbar_try_wait, but a thread whose phase has not completed is suspended by the hardware until it
-// completes or `ns` nanoseconds pass (the suspend-time hint), instead of returning after the default
-// short limit: waiting warps then take no issue slots from the working ones.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.b32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
-      : "memory");
-  return ok != 0;
-}
-
 // Non-blocking test of three barriers at once (the three tests are independent, so their
 // shared-memory round trips overlap); true when all three phases have completed.
 __device__ __forceinline__ bool mbar_test3(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb, uint64_t* c,

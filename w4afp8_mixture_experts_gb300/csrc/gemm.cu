@@ -55,6 +55,7 @@
 //     experts in between; split-K with fp32 partials for dense Linear calls
 //     whose tiles leave SMs idle.
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 
@@ -71,7 +72,6 @@ constexpr int kWarpMma = 2;                  // warps 2 .. 1 + kMmaWarps issue t
 constexpr int kConvWarps = 4;                // converter warps per set: one per tensor-memory lane quarter
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxDynSmem = 227 * 1024;  // dynamic shared memory a CTA may use on sm_100 / sm_103
-constexpr int kSmallExpertRows = 16;  // grouped GEMM with many rows: experts up to this many rows take 16-wide tiles
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s: no legitimate wait comes close
 
 __device__ unsigned int g_gemm_error;
@@ -1156,6 +1156,79 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
   }
 }
 
+// Tile-cost model of the two token-tile widths of the grouped GEMM, the per-expert expected-cost
+// choice of the DeepGEMM PR #53 page (Conversation, the cost-model commit: a tile width's cost is
+// a * R + b * T with T the tiles and R the rows they pad to, taken in expectation over Poisson row
+// counts), restated for these kernels.  Units: one 16-wide tile's time at the same N and K (weight
+// streaming dominates it).  A 128-wide tile converts the same weights and promotes up to eight times
+// the columns.  cost_W(x) = b_W * T_W(x) + a_W * R_W(x), T_W = ceil(x / W), R_W = rows padded to
+// 16 within each tile; fitted to GB300 sweeps of 256 experts with x rows each at (N, K) = (4096,
+// 7168) and (7168, 2048), x = 1 ... 256, to within ~10 %: narrow a = 0, b = 1; wide a = 0.004, b = 2.
+struct TileCost {
+  double a, b;
+  int width;
+};
+constexpr TileCost kNarrowCost{0.0, 1.0, 16};
+constexpr TileCost kWideCost{0.004, 2.0, 128};
+// The start-up of one more launch (~15 us of the whole GPU) in 16-wide tile times per weight block of
+// all E experts: a 16-wide tile takes ~1.8 ns per K on one SM.
+double launch_cost_tiles(int64_t E, int64_t K, int sms) {
+  const double tile_us = 1.8e-3 * static_cast<double>(K);
+  return 15.0 * sms / tile_us / static_cast<double>(E);
+}
+
+double tile_cost(int wide, int64_t x) {
+  const TileCost& c = wide ? kWideCost : kNarrowCost;
+  if (x <= 0) return 0.0;
+  const int64_t full = x / c.width, rem = x - full * c.width;
+  const int64_t T = full + (rem > 0 ? 1 : 0);
+  const int64_t R = full * c.width + (rem + 15) / 16 * 16;
+  return c.b * static_cast<double>(T) + c.a * static_cast<double>(R);
+}
+
+// The largest row count of one expert for which the narrow tiles cost no more than the wide ones.
+int crossover_rows() {
+  int x = 1;
+  while (x <= 128 && tile_cost(0, x) <= tile_cost(1, x)) ++x;
+  return x - 1;
+}
+
+// E[cost_W(X) ; lo <= X <= hi] for X ~ Poisson(lambda), summed until the tail is negligible.
+double expected_cost(int wide, double lambda, int64_t lo, int64_t hi) {
+  if (lambda <= 0.0) return 0.0;
+  const int64_t top = static_cast<int64_t>(lambda + 12.0 * std::sqrt(lambda) + 40.0);
+  double sum = 0.0, logp = -lambda;  // log P(X = 0)
+  for (int64_t x = 1; x <= top && x <= hi; ++x) {
+    logp += std::log(lambda) - std::log(static_cast<double>(x));
+    if (x >= lo) sum += std::exp(logp) * tile_cost(wide, x);
+  }
+  return sum;
+}
+
+constexpr int kPlanNarrow = 1, kPlanWide = 2, kPlanSplit = 3;
+
+// Launch plan of a grouped GEMM from what the host knows (M rows over E experts, K): the expected
+// cost per expert of each plan under Poisson(M / E) row counts, plus one launch start-up for the
+// split plan (narrow tiles for experts with at most theta rows, wide ones for the rest, in two
+// launches; the device applies the threshold to the realised row counts).  Poisson counts describe
+// balanced routing only; when the mean lies between the crossover and the wide tile (theta * E < M <
+// 128 * E), a skewed batch has experts on both sides, so the split plan is kept there: it costs at
+// most one start-up more than the Poisson optimum (skewed layer 4.13 -> 3.81 ms).
+int plan_grouped(int64_t M, int64_t E, int64_t K, int* theta_out) {
+  const int theta = crossover_rows();
+  if (theta_out) *theta_out = theta;
+  const double lambda = static_cast<double>(M) / static_cast<double>(E);
+  const double inf = 1e18;
+  const double narrow = expected_cost(0, lambda, 1, static_cast<int64_t>(inf));
+  const double wide = expected_cost(1, lambda, 1, static_cast<int64_t>(inf));
+  const double split = expected_cost(0, lambda, 1, theta) + expected_cost(1, lambda, theta + 1, static_cast<int64_t>(inf)) +
+                       launch_cost_tiles(E, K, num_sms());
+  int best = narrow <= wide ? kPlanNarrow : kPlanWide;
+  if (split < std::min(narrow, wide)) best = kPlanSplit;
+  if (best != kPlanSplit && M > static_cast<int64_t>(theta) * E && M < 128 * E) best = kPlanSplit;
+  return best;
+}
+
 // K splits the dense Linear uses for this shape on the current device (1: none).
 int linear_splits(int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0 || N % kBM || K % kGroup) return 1;
@@ -1192,25 +1265,21 @@ int gemm_common(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_
     if ((rc = launch_gcorr(A, M, K, a_s, a_ld, corr, st))) return rc;
     a_c = corr;
   }
-  // Few rows per expert: weight streaming, 16-wide token tiles and a deep ring.
-  if (M <= 32 * E && seg && K >= 4096)
-    rc = launch<CfgDecodeLongK>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st);
-  else if (M <= 32 * E)
-    rc = launch<CfgDecode>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st);
-  else if (seg && M < 128 * E) {
-    // Fewer rows than one 128-wide tile per expert on average, so (skewed routing) many experts may hold
-    // only a few: experts with at most kSmallExpertRows rows take the 16-wide tiles, the rest the
-    // 128-wide ones, in two launches over disjoint experts.  A 128-wide tile converts and promotes as
-    // much for 5 rows as for 128 (skewed layer 4.13 -> 3.81 ms).  With more rows per expert the second
-    // launch would mostly find nothing to do and cost its start-up (~20 us).
-    rc = K >= 4096 ? launch<CfgDecodeLongK>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st, 1,
-                                            kSmallExpertRows)
-                   : launch<CfgDecode>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st, 1,
-                                       kSmallExpertRows);
-    if (rc == W4A8_OK)
-      rc = launch<CfgPrefill>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st, kSmallExpertRows + 1);
-  } else
-    rc = launch<CfgPrefill>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st);
+  // The dense Linear: 16-wide token tiles (weight streaming) up to 32 rows, 128-wide above.  The grouped
+  // GEMM: the cost-model plan (narrow, wide, or both over disjoint experts split at theta rows).
+  int theta = 0;
+  const int plan = seg ? plan_grouped(M, E, K, &theta) : (M <= 32 ? kPlanNarrow : kPlanWide);
+  const int narrow_max = plan == kPlanSplit ? theta : 0x7fffffff;
+  if (plan != kPlanWide) {
+    rc = K >= 4096 && seg ? launch<CfgDecodeLongK>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st, 1,
+                                                   narrow_max)
+                          : launch<CfgDecode>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st, 1,
+                                              narrow_max);
+    if (rc != W4A8_OK) return rc;
+  }
+  if (plan != kPlanNarrow)
+    rc = launch<CfgPrefill>(A, a_s, a_c, a_ld, B, b_s, seg, E, N, K, M, C, partial, S, st,
+                            plan == kPlanSplit ? theta + 1 : 1);
   if (rc != W4A8_OK || S == 1) return rc;
   const int64_t MN = M * N;  // N % 128 == 0, so MN % 4 == 0
   const int64_t blocks = ceil_div(MN / 4, 256) < 8 * 152 ? ceil_div(MN / 4, 256) : 8 * 152;
@@ -1251,6 +1320,17 @@ extern "C" int w4a8_linear(const uint8_t* A, const float* a_scales, const float*
 }
 
 extern "C" int w4a8_linear_split_k(int64_t M, int64_t N, int64_t K) { return w4a8::linear_splits(M, N, K); }
+
+extern "C" double w4a8_tile_cost(int wide, int64_t rows) { return w4a8::tile_cost(wide, rows); }
+
+extern "C" double w4a8_expected_tile_cost(int wide, double mean_rows) {
+  return w4a8::expected_cost(wide, mean_rows, 1, 1ll << 40);
+}
+
+extern "C" int w4a8_grouped_gemm_plan(int64_t M_total, int64_t E, int64_t K, int* theta) {
+  if (M_total <= 0 || E < 1 || K <= 0) return 0;
+  return w4a8::plan_grouped(M_total, E, K, theta);
+}
 
 extern "C" int w4a8_prepack_weights(const uint8_t* w, int64_t rows, int64_t K, uint8_t* out, void* stream) {
   using namespace w4a8;
