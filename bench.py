@@ -13,8 +13,8 @@ FP8 tensor roofline), weights 6.0 GB (larger than L2, so every step streams them
 line carries the decode layer (T=64, same experts, against the HBM roofline) under "decode", measured in
 the same process on the same weights.
 
---impl reference times the CPU oracle (numpy, float64, one thread) on a bounded
-sample of the same workload (a few tokens per step).
+--impl reference times the CPU oracle (numpy, float64) over the host's cores (one process with one BLAS
+thread per core, spawn-started) on a bounded sample of the same workload (a few tokens per core per step).
 """
 from __future__ import annotations
 
@@ -693,15 +693,15 @@ def run_linear(args, cfg, dev, world, rank, peaks, peak_src):
 # ---------------------------------------------------------------------------
 # CPU oracle (reference arm and cpu_baseline)
 
-def oracle_sample(name, cfg, seed, n_tokens):
-    """Host inputs and weights of a token sample; returns a closure running the oracle on it."""
+def oracle_sample(name, cfg, seed, tokens):
+    """Host inputs and weights of a token sample (token indices `tokens`); returns a closure running the
+    oracle on it.  The weights are generated here, before any timing (model parameters in memory)."""
     import oracle
     from helpers import moe_experts, moe_host_inputs
     x_bits, logits = moe_host_inputs(seed, cfg)
     x = inputs.bf16_bits_to_f32(x_bits)
     w13, w2 = moe_experts(seed, cfg)
-    sel = np.arange(n_tokens)
-    # weights are model parameters already in memory: generate them before timing
+    sel = np.asarray(tokens)
     ids, _ = oracle.route_topk(logits[sel], cfg["k"])
     emap, glob = None, np.arange(cfg["E"])
     if cfg.get("ep"):  # one expert-parallel shard: local id l is global expert r + l*R
@@ -713,15 +713,66 @@ def oracle_sample(name, cfg, seed, n_tokens):
     loc = {(int(emap[e]) if emap is not None else e): e for e in used}
     cache13 = {l: (w13.w(e), w13.s(e)) for l, e in loc.items()}
     cache2 = {l: (w2.w(e), w2.s(e)) for l, e in loc.items()}
+    xs, lgs = x[sel], logits[sel]
 
     def run():
-        return oracle.moe_tokens(x[sel], logits[sel], cfg["k"], lambda e: cache13[e][0], lambda e: cache13[e][1],
+        return oracle.moe_tokens(xs, lgs, cfg["k"], lambda e: cache13[e][0], lambda e: cache13[e][1],
                                  lambda e: cache2[e][0], lambda e: cache2[e][1], expert_map=emap)
     return run
 
 
+def _oracle_worker(name, cfg, seed, tokens, core, rounds, barrier, out):
+    """One host core of the CPU baseline: prepares its tokens' sample, then for each round waits for every
+    worker (barrier) and times the oracle on its tokens."""
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[v] = "1"
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    try:
+        mine = sorted(os.sched_getaffinity(0))
+        os.sched_setaffinity(0, {mine[core % len(mine)]})
+    except (AttributeError, OSError):
+        pass
+    run = oracle_sample(name, cfg, seed, tokens)
+    for _ in range(rounds):
+        barrier.wait()
+        t = time.perf_counter()
+        run()
+        out.put(time.perf_counter() - t)
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_on_host_cores(name, cfg, seed, per_core, rounds, cores=None):
+    """The oracle over `cores` processes (spawn start; one BLAS thread each), `per_core` tokens each, the
+    cores' token samples disjoint; every round starts on all cores together.  Returns the wall time of
+    each round (the slowest core's) and the number of tokens a round processes."""
+    import multiprocessing as mp
+    cores = cores or host_cores()
+    T = cfg["T"]
+    ctx = mp.get_context("spawn")
+    barrier, out = ctx.Barrier(cores), ctx.Queue()
+    procs = []
+    for c in range(cores):
+        tokens = [(c * per_core + i) % T for i in range(per_core)]
+        p = ctx.Process(target=_oracle_worker, args=(name, cfg, seed, tokens, c, rounds, barrier, out), daemon=True)
+        p.start()
+        procs.append(p)
+    per_round = []
+    for _ in range(rounds):
+        per_round.append(max(out.get(timeout=900) for _ in range(cores)))
+    for p in procs:
+        p.join(timeout=60)
+    return per_round, cores * per_core, cores
+
+
 def default_cpu_tokens(name):
-    return {"tiny": 64, "decode": 1, "prefill": 1, "skewed": 1}.get(name, 8 if name.startswith("ep-") else 1)
+    return {"tiny": 64}.get(name, 1)
 
 
 def run_reference(args, name, cfg):
@@ -732,42 +783,37 @@ def run_reference(args, name, cfg):
         print(json.dumps({"impl": "reference", "unavailable": "the reference arm covers the MoE workloads"}))
         return
     n = args.cpu_tokens or default_cpu_tokens(name)
-    times = []
-    run = oracle_sample(name, cfg, args.seed, n)  # inputs and weights prepared once, untimed
-    for i in range(args.warmup + args.steps):
-        t = time.perf_counter()
-        run()
-        dt = time.perf_counter() - t
-        if i >= args.warmup:
-            times.append(dt)
+    rounds, tokens, cores = oracle_on_host_cores(name, cfg, args.seed, n, args.warmup + args.steps)
+    times = rounds[args.warmup:]
     tot = sum(times)
-    value = n * len(times) / tot
+    value = tokens * len(times) / tot
     res = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": 1,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot / len(times), 2),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {"workload": workload_desc(name, cfg)},
-           "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                            "sample": f"{n} token(s) of the workload per step ({n * cfg['k']} routed pairs"
-                                      f"{', those of the shard computed' if cfg.get('ep') else ''}), "
-                                      f"numpy float64, one BLAS thread"},
+           "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                            "sample": f"{tokens} token(s) of the workload per step, {n} on each of {cores} host "
+                                      f"cores ({n * cfg['k']} routed pairs per core"
+                                      f"{', those of the shard computed' if cfg.get('ep') else ''}), numpy "
+                                      f"float64, one BLAS thread per process, rounds started together"},
            "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
 
 
 def cpu_baseline(name, spec, args):
-    """The oracle in a single-threaded child process on a bounded sample (~10-30 s)."""
-    n = {"tiny": 64}.get(name, 32 if name.startswith("ep-") else 4)
+    """The oracle over the host's cores on a bounded sample (~10-30 s), in a child process."""
+    n = {"tiny": 8}.get(name, 4 if name.startswith("ep-") else 2)
     cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--workload", spec, "--steps", "1",
            "--warmup", "0", "--cpu-tokens", str(n), "--seed", str(args.seed)]
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
     for v in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
         env.pop(v, None)
     try:
-        out = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=600).stdout.strip().splitlines()
+        out = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900).stdout.strip().splitlines()
         d = json.loads(out[-1])
         return d["cpu_baseline"]
     except Exception as e:  # reported, never fatal for the GPU number
-        return {"value": None, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": f"failed: {e}"}
+        return {"value": None, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle", "sample": f"failed: {e}"}
 
 
 def main():

@@ -175,7 +175,7 @@ def test_peaks_file_has_the_fields_the_bench_reads():
 def test_default_cpu_sample_sizes():
     assert bench.default_cpu_tokens("tiny") == 64
     assert bench.default_cpu_tokens("decode") == 1
-    assert bench.default_cpu_tokens("ep-prefill") == 8
+    assert bench.default_cpu_tokens("ep-prefill") == 1
     assert np.isfinite(bench.throughput(1, 1, 1.0))
 
 
@@ -228,3 +228,11 @@ def test_clock_rows_summary_names_the_rejecting_reasons():
     out = bench.summarize_clock_rows(rows, 2070, bench.NvmlSampler.REASONS)
     assert out["sm_mhz"] == 1800 and out["power_w_max"] == 1400.0 and out["samples"] == 4
     assert out["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_power_cap", "sw_thermal_slowdown"]
+
+
+def test_oracle_over_host_cores_runs_rounds_together():
+    # two spawn-started processes, one token each of the tiny layer, two rounds
+    cfg = dict(inputs.WORKLOADS["tiny"])
+    rounds, tokens, cores = bench.oracle_on_host_cores("tiny", cfg, 0, 1, 2, cores=2)
+    assert len(rounds) == 2 and tokens == 2 and cores == 2
+    assert all(0.0 < r < 60.0 for r in rounds)
