@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="prefill: leave out the decode layer's keys")
+    ap.add_argument("--fused-w13", action="store_true",
+                    help="time w13 with the SiLU-and-Mul requantisation fused into its epilogue")
     ap.add_argument("--sustain-s", type=float, default=1.5,
                     help="seconds of untimed steps after the timed region with the clocks sampled (0: none)")
     ap.add_argument("--cpu-tokens", type=int, default=0, help="tokens per oracle step (0: automatic)")
@@ -281,7 +283,7 @@ def throughput(units_per_rank: float, world: int, max_ms: float) -> float:
 # ---------------------------------------------------------------------------
 # algorithmic work and rooflines (host arithmetic only)
 
-def moe_counts(T, H, I, E, k, P, n_touched):
+def moe_counts(T, H, I, E, k, P, n_touched, fused=False):
     """Algorithmic work of one MoE layer step over P routed pairs, n_touched of the E experts holding any.
 
     FLOPs count the routed pairs only (no padding).  Bytes count the int4 weights and fp32 per-128 scales of
@@ -290,9 +292,12 @@ def moe_counts(T, H, I, E, k, P, n_touched):
     """
     w13_w = n_touched * (2 * I * H // 2 + 2 * I * (H // 128) * 4)
     w2_w = n_touched * (H * I // 2 + H * (I // 128) * 4)
+    # with SiLU-and-Mul fused into w13's epilogue the launch writes the requantised h (codes, scales and
+    # corrections) instead of Y13
+    out13 = P * I + 2 * (I // 128) * P * 4 if fused else P * 2 * I * 2
     return {"flops": 2.0 * P * (2 * I * H + I * H),
             "layer_bytes": w13_w + w2_w + T * H * 2 + T * E * 4 + T * H * 2,
-            "w13_bytes": w13_w + P * H + (H // 128) * P * 4 + P * 2 * I * 2,
+            "w13_bytes": w13_w + P * H + (H // 128) * P * 4 + out13,
             "w13_flops": 2.0 * P * 2 * I * H}
 
 
@@ -308,6 +313,16 @@ def moe_launches_per_step(n_stages, two_pass_permute, gemm_plans):
     plus a second launch for each grouped GEMM whose plan (w4a8_grouped_gemm_plan: 1 narrow tiles, 2 wide
     tiles, 3 both over disjoint experts) is the split one."""
     return n_stages + (1 if two_pass_permute else 0) + sum(1 for p in gemm_plans if p == 3)
+
+
+def w13_fuses(lib, pairs, experts, H):
+    """Whether the layer's w13 launch carries the SiLU-and-Mul requantisation (the wide-tile plan with two or
+    more stages of two 128-K groups per tile)."""
+    import ctypes
+    th = ctypes.c_int()
+    G = H // 128
+    gps = 2 if G % 2 == 0 else 1
+    return int(lib.w4a8_grouped_gemm_plan(pairs, experts, H, ctypes.byref(th))) == 2 and G // gps >= 2
 
 
 def gemm_plans(lib, pairs, experts, H, I):
@@ -384,6 +399,9 @@ class MoeRunner:
                                                  "xq", "xs", "xc", "y13", "hq", "hs", "hc", "y2", "permute_ws")}
         self.permute_ws_bytes = int(m.load().w4a8_workspace_bytes(1, T * k, 0, 0, self.EL))
         self.ld = L.scale_ld
+        # --fused-w13: w13 through w4a8_grouped_gemm_silu, the SiLU-and-Mul requantisation in its epilogue where
+        # the plan allows (w4a8_moe_forward keeps the separate kernel, which measured faster)
+        self.fused = bool(cfg.get("fused_w13")) and (not self.ep) and w13_fuses(self.lib, T * k, E, H)
 
     def stages(self, stream):
         """The seven calls of one step, as closures (each returns a status)."""
@@ -410,15 +428,24 @@ class MoeRunner:
                 ("combine", lambda: lib.moe_unpermute_combine(p["y2"], p["src2dst"], p["topk_w"], T, k, H, out,
                                                               stream)),
             ]
-        return [
+        head = [
             ("route", lambda: lib.moe_route_topk(lg, T, E, k, 1, p["topk_ids"], p["topk_w"], stream)),
             ("permute", lambda: lib.moe_permute(p["topk_ids"], T, k, E, p["seg_indptr"], p["src2dst"],
                                                 p["dst2src"], p["permute_ws"], self.permute_ws_bytes, stream)),
             ("quant", lambda: lib.fp8_quant_scatter_per_token_group(x, T, H, p["src2dst"], k, P, p["xq"], p["xs"],
                                                                     p["xc"], ld, stream)),
-            ("w13", lambda: lib.w4a8_grouped_gemm(p["xq"], p["xs"], p["xc"], ld, w13, w13s, p["seg_indptr"], E,
-                                                  2 * I, H, P, p["y13"], None, 0, stream)),
-            ("silu_requant", lambda: lib.silu_mul_requant(p["y13"], P, I, p["hq"], p["hs"], p["hc"], ld, stream)),
+        ]
+        if self.fused:  # w13 with the SiLU-and-Mul requantisation in its epilogue, as w4a8_moe_forward runs it
+            mid = [("w13", lambda: lib.w4a8_grouped_gemm_silu(p["xq"], p["xs"], p["xc"], ld, w13, w13s,
+                                                              p["seg_indptr"], E, I, H, P, p["hq"], p["hs"],
+                                                              p["hc"], ld, p["y13"], self.L.hq - self.L.y13,
+                                                              stream))]
+        else:
+            mid = [("w13", lambda: lib.w4a8_grouped_gemm(p["xq"], p["xs"], p["xc"], ld, w13, w13s, p["seg_indptr"],
+                                                         E, 2 * I, H, P, p["y13"], None, 0, stream)),
+                   ("silu_requant", lambda: lib.silu_mul_requant(p["y13"], P, I, p["hq"], p["hs"], p["hc"], ld,
+                                                                 stream))]
+        return head + mid + [
             ("w2", lambda: lib.w4a8_grouped_gemm(p["hq"], p["hs"], p["hc"], ld, w2, w2s, p["seg_indptr"], E, H, I,
                                                  P, p["y2"], None, 0, stream)),
             ("combine", lambda: lib.moe_unpermute_combine(p["y2"], p["src2dst"], p["topk_w"], T, k, H, out,
@@ -466,6 +493,8 @@ def run_ours(args, name, cfg):
     seed = args.seed + rank
     if name == "linear":
         return run_linear(args, cfg, dev, world, rank, peaks, peak_src)
+    if args.fused_w13:
+        cfg = dict(cfg, fused_w13=True)
     r = MoeRunner(cfg, seed, dev)
     res = measure_moe(r, name, cfg, args, dev, world, peaks, peak_src)
     if not args.no_e2e:
@@ -572,12 +601,14 @@ def measure_moe(r, name, cfg, args, dev, world, peaks, peak_src):
     P = int(seg[-1])  # routed pairs computed (all T*k, or the shard's)
     ms_step = ms / K
     value = throughput(T * K, world, ms)
-    cnt = moe_counts(T, H, I, E, k, P, n_touched)
+    cnt = moe_counts(T, H, I, E, k, P, n_touched, fused=r.fused)
     flops, layer_bytes = cnt["flops"], cnt["layer_bytes"]
     # dominant kernel: the w13 grouped GEMM, timed inside the long step (sustained tensor peak)
     roof = roofline_core(cnt["w13_bytes"], cnt["w13_flops"], w13_timed_ms, peaks["hbm_gbs"],
                          FP8_OVER_BF16 * peaks["bf16_tflops_sustained"])
-    roof.update({"traffic": ncu_traffic(f"{name}:w13"), "kernel": "w4a8_gemm_kernel (w13 grouped GEMM)"})
+    roof.update({"traffic": ncu_traffic(f"{name}:w13"),
+                 "kernel": "w4a8_gemm_kernel (w13 grouped GEMM" + (", SiLU-and-Mul requantisation fused)" if r.fused
+                                                                    else ")")})
     if roof["bound"] == "hbm":
         roof.update({"algorithmic_bytes": int(cnt["w13_bytes"]), "peak_source": f"{peak_src} hbm_gbs"})
     else:

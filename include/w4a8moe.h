@@ -196,6 +196,36 @@ int w4a8_grouped_gemm(const uint8_t* A, const float* a_scales, const float* a_gc
                       uint16_t* C, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * (4) for w13 followed by (5), with N = 2I: q, h_scales, h_gcorr are what
+ * silu_mul_requant writes for the Y13 that (4) computes (gate rows [0, I),
+ * up rows [I, 2I) of each expert's w13).  When the plan of (4) takes the
+ * 128-row tiles only, the SiLU and Mul with FP8 requantisation runs in the
+ * GEMM's epilogue (the fused L1 epilogue of the DeepGEMM PR #53 page, Changes:
+ * L1 GEMM -> SwiGLU -> per-token FP8 requant): a CTA computes the gate block
+ * and the up block of the same 128 h-columns in turn, rounds both to bf16
+ * (as Y13 would hold them), and forms h, the 128-column amax, the codes, the
+ * scale and the correction with the SiLU-and-Mul kernel's arithmetic, so the
+ * results equal the unfused ones bit for bit; Y13 is not written.  Otherwise
+ * (4) writes Y13 into ws and (5) reads it.
+ *   A, a_scales, a_gcorr (may be NULL), B_prepacked, b_scales, seg_indptr, E, K,
+ *   M_total as in (4) with N = 2I   q uint8 [M_total][I] (16-byte aligned)
+ *   h_scales, h_gcorr fp32 [I/128][h_scale_ld] (h_gcorr may be NULL)
+ *   ws: w4a8_workspace_bytes(W4A8_OP_GROUPED_GEMM_SILU, M_total, 2I, K, E)
+ *   bytes, 16-byte aligned (Y13 [M_total][2I] bf16, or the bf16 gate values of
+ *   the fused epilogue, then the corrections of A when a_gcorr is NULL).
+ */
+int w4a8_grouped_gemm_silu(const uint8_t* A, const float* a_scales, const float* a_gcorr, int64_t a_scale_ld,
+                           const uint8_t* B_prepacked, const float* b_scales, const int64_t* seg_indptr, int64_t E,
+                           int64_t I, int64_t K, int64_t M_total, uint8_t* q, float* h_scales, float* h_gcorr,
+                           int64_t h_scale_ld, void* ws, size_t ws_bytes, void* stream);
+/* The same with the fusion switched off (always (4) then (5)); for comparisons. */
+int w4a8_grouped_gemm_silu_unfused(const uint8_t* A, const float* a_scales, const float* a_gcorr,
+                                   int64_t a_scale_ld, const uint8_t* B_prepacked, const float* b_scales,
+                                   const int64_t* seg_indptr, int64_t E, int64_t I, int64_t K, int64_t M_total,
+                                   uint8_t* q, float* h_scales, float* h_gcorr, int64_t h_scale_ld, void* ws,
+                                   size_t ws_bytes, void* stream);
+
+/*
  * One-time weight re-layout for the GEMMs (the post-load weight processing of
  * the PR #7762 page, process_weights_after_loading).  Canonical packed int4
  * rows [rows][K/2] -> prepacked rows of the same shape: within each 32-bit
@@ -285,6 +315,7 @@ double w4a8_expected_tile_cost(int wide, double mean_rows);
 #define W4A8_OP_PERMUTE 1
 #define W4A8_OP_GROUPED_GEMM 2
 #define W4A8_OP_LINEAR 3
+#define W4A8_OP_GROUPED_GEMM_SILU 4
 
 /* Workspace (bytes) an operation needs for the given shape; 0 = none. */
 size_t w4a8_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int64_t E);

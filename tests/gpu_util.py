@@ -77,3 +77,4 @@ def decode_prepacked(words_u8):
         half2 = np.where(s == 1, -(2 * m + 1), 2 * m + 1)  # 2 * (v + 1/2)
         out[..., e] = (half2 - 1) // 2
     return out.reshape(words_u8.shape[:-1] + (words_u8.shape[-1] * 2,))
+

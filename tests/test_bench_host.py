@@ -59,6 +59,15 @@ def test_expert_bytes_and_layer_flops_closed_forms():
     assert c["w13_flops"] == pytest.approx(c["flops"] * 2 / 3)
 
 
+def test_fused_w13_writes_h_instead_of_y13():
+    H, I = 256, 512
+    a = bench.moe_counts(4, H, I, 8, 2, 10, 3)
+    b = bench.moe_counts(4, H, I, 8, 2, 10, 3, fused=True)
+    # Y13 (2I bf16 per pair) replaced by I E4M3 codes + I/128 scales and corrections per pair
+    assert a["w13_bytes"] - b["w13_bytes"] == 10 * (2 * I * 2 - I - 2 * (I // 128) * 4)
+    assert a["w13_flops"] == b["w13_flops"] and a["flops"] == b["flops"]
+
+
 def test_w13_bytes_add_activation_traffic_per_pair():
     H, I = 256, 512
     base = bench.moe_counts(4, H, I, 8, 2, 0, 3)["w13_bytes"]

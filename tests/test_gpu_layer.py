@@ -52,6 +52,7 @@ def _ws_view(ws, off, dtype, shape):
     ("k-equals-E", dict(T=20, H=128, I=128, E=3, k=3)),
     ("many-experts", dict(T=200, H=512, I=384, E=160, k=6)),
     ("prefill-tiles", dict(T=700, H=256, I=256, E=4, k=2)),
+    ("wide-two-stages", dict(T=600, H=512, I=256, E=4, k=2)),
 ])
 def test_layer_stage_by_stage(lib, name, cfg):
     seed = 3
@@ -82,8 +83,8 @@ def test_layer_stage_by_stage(lib, name, cfg):
     assert np.array_equal(xq, rq[tok]) and np.array_equal(xs, rs[tok])
     assert np.array_equal(xc, gcorr_of(xq, xs))  # exact code sums, then one fp32 product
     # (4) w13 on the device's own inputs (identical to the oracle's): 1e-3
-    y13 = _ws_view(ws, L.y13, torch.bfloat16, (P, 2 * I)).float().numpy().astype(np.float64)
     ry13 = oracle.round_bf16(oracle.grouped_gemm(xq, xs, seg, w13h.w, w13h.s))
+    y13 = _ws_view(ws, L.y13, torch.bfloat16, (P, 2 * I)).float().numpy().astype(np.float64)
     assert rel_fro(y13, ry13) <= 1e-3
     # (5) SiLU-and-Mul requant of the device's Y13
     hq = _ws_view(ws, L.hq, torch.uint8, (P, I)).numpy()

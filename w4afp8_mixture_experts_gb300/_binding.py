@@ -35,6 +35,10 @@ _SIGS = {
     "w4a8_grouped_gemm": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64,
                                    _c_i64, _c_vp, _c_vp, _c_sz, _c_vp]),
     "w4a8_prepack_weights": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_vp]),
+    "w4a8_grouped_gemm_silu": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_i64,
+                                        _c_i64, _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_sz, _c_vp]),
+    "w4a8_grouped_gemm_silu_unfused": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64, _c_i64,
+                                                _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_sz, _c_vp]),
     "silu_mul_requant": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64, _c_vp]),
     "silu_mul_requant_rows": (_c_int, [_c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64, _c_vp]),
     "moe_unpermute_combine": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_int, _c_i64, _c_vp, _c_vp]),
@@ -227,6 +231,36 @@ def w4a8_grouped_gemm(A, a_scales, a_gcorr, B_prepacked, b_scales, seg_indptr):
                                     _p(b_scales), _p(seg_indptr), E, N, K, M, _p(C), _p(ws),
                                     0 if ws is None else ws.numel(), _stream()))
     return C
+
+
+def w4a8_grouped_gemm_silu(A, a_scales, a_gcorr, B_prepacked, b_scales, seg_indptr, fused: bool = True):
+    """The w13 grouped GEMM (B_prepacked [E, 2I, K/2]: gate rows then up rows) followed by SiLU-and-Mul
+    requantisation -> (codes uint8 [M, I], scales fp32 [I/128, ld], gcorr fp32 [I/128, ld]).  With
+    fused=True the requantisation runs in the GEMM's epilogue when the tile plan allows (same bits)."""
+    _req(A, torch.uint8, "A", 2)
+    _req(a_scales, torch.float32, "a_scales", 2)
+    if a_gcorr is not None:
+        _req(a_gcorr, torch.float32, "a_gcorr", 2)
+    _req(B_prepacked, torch.uint8, "B_prepacked", 3)
+    _req(b_scales, torch.float32, "b_scales", 3)
+    _req(seg_indptr, torch.int64, "seg_indptr", 1)
+    M, K = A.shape
+    E, N, Kh = B_prepacked.shape
+    if Kh * 2 != K or seg_indptr.numel() != E + 1 or N % 256:
+        raise ValueError("shape mismatch")
+    I = N // 2
+    ld = scale_ld(M)
+    need = int(load().w4a8_workspace_bytes(4, M, N, K, E))
+    if a_gcorr is None:
+        need += (K // 128) * (a_scales.shape[1] - scale_ld(M)) * 4
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=A.device)
+    q = torch.empty((M, I), dtype=torch.uint8, device=A.device)
+    s = torch.empty((I // 128, ld), dtype=torch.float32, device=A.device)
+    c = torch.empty((I // 128, ld), dtype=torch.float32, device=A.device)
+    fn = load().w4a8_grouped_gemm_silu if fused else load().w4a8_grouped_gemm_silu_unfused
+    _check(fn(_p(A), _p(a_scales), _p(a_gcorr), a_scales.shape[1], _p(B_prepacked), _p(b_scales), _p(seg_indptr), E,
+              I, K, M, _p(q), _p(s), _p(c), ld, _p(ws), ws.numel(), _stream()))
+    return q, s, c
 
 
 def silu_mul_requant(gate_up):

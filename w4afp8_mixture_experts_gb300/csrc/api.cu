@@ -111,6 +111,7 @@ extern "C" int w4a8_device_error(void) {
 extern "C" size_t w4a8_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int64_t E) {
   if (op == W4A8_OP_LINEAR) return w4a8::gemm_workspace_bytes(M, N, K, true);
   if (op == W4A8_OP_GROUPED_GEMM) return w4a8::gemm_workspace_bytes(M, N, K, false);
+  if (op == W4A8_OP_GROUPED_GEMM_SILU) return w4a8::gemm_silu_workspace_bytes(M, N, K);
   if (op == W4A8_OP_PERMUTE) return w4a8::permute_ws_bytes(M, E);
   return 0;
 }
@@ -155,6 +156,9 @@ extern "C" int w4a8_moe_forward(const uint16_t* x, const float* logits, int64_t 
   if ((rc = moe_route_topk(logits, T, E, k, renormalize, ids, tw, stream))) return rc;
   if ((rc = moe_permute(ids, T, k, E, seg, s2d, d2s, b + L.permute_ws, permute_ws_bytes(P, E), stream))) return rc;
   if ((rc = fp8_quant_scatter_per_token_group(x, T, H, s2d, k, P, xq, xs, xc, L.scale_ld, stream))) return rc;
+  // w13, then SiLU-and-Mul requantisation in its own kernel: with the requantisation fused into w13's
+  // epilogue (w4a8_grouped_gemm_silu) the prefill w13 launch took 5.37 ms against 4.22 + 0.19 ms, since
+  // the promotion epilogue is the GEMM's critical role and the SiLU math is cheaper at full occupancy
   if ((rc = w4a8_grouped_gemm(xq, xs, xc, L.scale_ld, w13, w13_s, seg, E, 2 * I, H, P, y13, nullptr, 0, stream)))
     return rc;
   if ((rc = silu_mul_requant(y13, P, I, hq, hs, hc, L.scale_ld, stream))) return rc;

@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -74,6 +75,8 @@ size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 // workspace of a GEMM call that also computes the activation corrections itself (a_gcorr NULL, scale
 // leading dimension M rounded up to 4): the split-K partial sums (dense only), then the corrections
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, bool dense);
+// workspace of w4a8_grouped_gemm_silu (N = 2 I): Y13 or the gate scratch, then the corrections
+size_t gemm_silu_workspace_bytes(int64_t M, int64_t N, int64_t K);
 // gcorr[g][m] of the E4M3 codes A [M][K] and their scales (the arithmetic of the quantisation kernels)
 int launch_gcorr(const uint8_t* A, int64_t M, int64_t K, const float* a_s, int64_t ld, float* gcorr,
                  cudaStream_t st);
@@ -109,6 +112,57 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// --- the quantisation arithmetic shared by the quantisation kernels and the fused GEMM epilogue ---------
+
+// x / s rounded to nearest even in fp32 from r = RN(1/s), by Markstein's correction step
+// (P. Markstein, "Computation of elementary functions on the IBM RISC System/6000 processor",
+// IBM J. Res. Dev. 34(1), 1990): if r is within half an ulp of 1/s and q within one ulp of x/s,
+// the residual e = x - q*s is exact in one fma and RN(q + e*r) is the correctly rounded
+// quotient.  RN(x*r) can be two ulps off (relative error up to 2^-23), so one correction first
+// brings it within an ulp and a second one rounds correctly.  Valid while nothing overflows or
+// underflows; quotients below 2^-10 all quantise to a signed E4M3 zero whatever their last
+// bits, so tiny x is harmless.
+// The steps need s and r = 1/s normal: amax >= 1e-12 keeps s >= 2.2e-15, and a finite amax keeps
+// r >= 2^-120; an infinite or NaN amax (r = 0 or NaN) takes the IEEE division instead.
+__device__ __forceinline__ float div_by_scale(float x, float s, float r) {
+  if (!(r > 0.0f && r < INFINITY)) return __fdiv_rn(x, s);
+  const float q0 = __fmul_rn(x, r);
+  const float q1 = __fmaf_rn(__fmaf_rn(-q0, s, x), r, q0);
+  // the sum of the correction can turn -0 into +0; the quotient's sign is x's (s > 0)
+  return copysignf(__fmaf_rn(__fmaf_rn(-q1, s, x), r, q1), x);
+}
+
+// One lane's share of a group's code sum, in units of 2^-9: every E4M3 value is a multiple of 2^-9
+// and at most 448 (229376 units), so the fp32 partial sum of a lane's at most 32 values stays on the
+// 2^-9 grid below 2^15 (24 significant bits) and it and its conversion to units are exact.
+template <int NW>
+__device__ __forceinline__ int code_units(const uint32_t (&code)[NW]) {
+  float sum = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NW; ++i)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      // E4M3 pairs -> f16 pairs (exact) -> fp32
+      uint32_t h2;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(code[i] >> (16 * h))));
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+      sum += f.x + f.y;
+    }
+  return __float2int_rn(sum * 512.0f);
+}
+
+// The group correction -1/2 * s * S from the exact code sum of the whole group, U units of 2^-9
+// (|U| < 2^25, an int32): S = U * 2^-9 is rounded to fp32 once (exact while |S| < 2^15), then one
+// rounded fp32 product with s; the halving is exact.
+__device__ __forceinline__ float corr_from_units(int units, float s) {
+  return -0.5f * __fmul_rn(s, __int2float_rn(units) * (1.0f / 512.0f));
+}
+
+// h = silu(gate) * up = gate / (1 + exp(-gate)) * up, fp32.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {

@@ -85,7 +85,7 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
 // Every consumer works on whole pipeline stages (GPS 128-K groups of one tile): a stage is
 // one barrier transaction for the converters, the MMA issue and the epilogue.
 template <int NMAX_, int GPS_, int STAGES_, int TSTAGES_, int SSTAGES_, int ABUF_, int NP_, bool A_TMEM_, int SETS_,
-          int MMAS_, int EPIW_, int EPIS_>
+          int MMAS_, int EPIW_, int EPIS_, bool FUSE_ = false>
 struct Cfg {
   // warp roles: 0 weight producer | 1 token/scale producer | 2..1+MMAS MMA issue | SETS x 4 converters |
   // EPIW epilogue
@@ -117,8 +117,15 @@ struct Cfg {
   static constexpr int kOffWpk = kOffTok + TSTAGES * GPS * kTokBytes;
   static constexpr int kOffA = kOffWpk + STAGES * GPS * kWpkBytes;
   static constexpr int kOffSc = kOffA + (A_TMEM ? 0 : ABUF * GPS * kABytes);
-  static constexpr int kOffBar = kOffSc + SSTAGES * kScBytes;
-  static constexpr int kNumBars = 2 * STAGES + 2 * TSTAGES + 2 * SSTAGES + 2 * ABUF + 2 * NP + 4;
+  // Fused SiLU-and-Mul requantisation (w13 only): gate and up tiles of the same 128 h-columns go to one
+  // CTA in turn; the up tile's epilogue needs the E4M3 codes of its NMAX tokens staged as rows
+  // [NMAX][kStageRow B] for coalesced stores, and per-lane-quarter partial amax and code sums [2][4][NMAX].
+  static constexpr bool kFuse = FUSE_;
+  static constexpr int kOffFuse = kOffSc + SSTAGES * kScBytes;
+  static constexpr int kStageRow = 144;  // staged code row: 128 B + 16 B of padding (byte stores spread over banks)
+  static constexpr int kFuseBytes = FUSE_ ? NMAX * kStageRow + 2 * 4 * NMAX * 4 : 0;
+  static constexpr int kOffBar = kOffFuse + kFuseBytes;
+  static constexpr int kNumBars = 2 * STAGES + 2 * TSTAGES + 2 * SSTAGES + 2 * ABUF + 2 * NP + 4 + (FUSE_ ? 2 : 0);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffSched = kOffMisc + 64;
   // schedule: [E+1] chunk prefix, [E+1] row starts, then (16-byte aligned) [cap] int4 tiles of this CTA
@@ -134,6 +141,7 @@ struct Cfg {
   static_assert(NMAX % 16 == 0 && NMAX >= 16 && NMAX <= 256, "token tile");
   static_assert(kTokBytes % 1024 == 0 && kOffWpk % 1024 == 0 && kOffA % 1024 == 0, "alignment");
   static_assert(kOffSc % 128 == 0 && kScBytes % 128 == 0, "TMA destinations 128-byte aligned");
+  static_assert(!FUSE_ || (NMAX_ == 128 && EPIS_ == 1 && EPIW_ == 8), "fused SiLU: 128-wide tiles, 8 epilogue warps");
   static_assert(kTmemUsed <= 512, "tensor memory");
   static_assert(EPIS_ == 1 || EPIS_ == 2, "one or two epilogue sets");
   static_assert(EPIW_ % (4 * EPIS_) == 0, "each epilogue set covers all four lane quarters");
@@ -179,6 +187,13 @@ struct GemmParams {
   int splits;          // K splits per tile (1: none)
   int tile_cap;        // tiles per CTA the shared-memory tile list holds (0: decode each tile in place)
   int min_rows, max_rows;  // experts with a row count outside [min_rows, max_rows] are left to another launch
+  // fused SiLU-and-Mul requantisation (N = 2 I): the gate tile's bf16 values go to gate [M][I] (scratch
+  // read back by the same threads), the up tile's epilogue writes hq [M][I] E4M3, hs / hc [I/128][h_ld]
+  uint16_t* gate;
+  uint8_t* hq;
+  float* hs;
+  float* hc;
+  int64_t h_ld;
 };
 
 // UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -235,6 +250,12 @@ struct Sched {
   const int4* tiles;  // this CTA's tiles {e, nb, row0, rows} in order, or nullptr (decode in place)
   int E, NMAX, nblk;
   int S, Gs, gps;     // K splits per tile, stages per tile, groups per stage
+  int pairs;          // 1: tiles come in (gate block p, up block p + nblk / 2) pairs, a pair to one CTA
+  // global item of this CTA's tile `it`: CTAs stride over items, or over pairs of items
+  __device__ __forceinline__ int item_of(int it) const {
+    return pairs ? 2 * (static_cast<int>(blockIdx.x) + (it >> 1) * static_cast<int>(gridDim.x)) + (it & 1)
+                 : static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x);
+  }
   // item = tile * S + split; split s covers stages [s*Gs/S, (s+1)*Gs/S) of the tile
   __device__ __forceinline__ void krange(int item, int& g_beg, int& g_end) const {
     const int sp = item % S;
@@ -243,8 +264,15 @@ struct Sched {
   }
   __device__ __forceinline__ void decode(int item_, int& e, int& nb, int& row0, int& rows) const {
     const int item = item_ / S;
-    const int chunk = item / nblk;
-    nb = item - chunk * nblk;
+    int chunk;
+    if (pairs) {  // item = 2 * (chunk * nblk / 2 + p) + half -> block p (gate) or p + nblk / 2 (up)
+      const int np = nblk >> 1, pi = item >> 1;
+      chunk = pi / np;
+      nb = pi - chunk * np + (item & 1) * np;
+    } else {
+      chunk = item / nblk;
+      nb = item - chunk * nblk;
+    }
     int lo = 0, hi = E;  // prefix[lo] <= chunk < prefix[hi]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -362,6 +390,7 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
   uint64_t* pempty = pfull + NP;        // [NP] partial slot read by the epilogue
   uint64_t* xfull = pempty + NP;        // [2] epilogue set 1 -> set 0 hand-over slot written
   uint64_t* xempty = xfull + 2;         // [2] hand-over slot read
+  uint64_t* hx = xempty + 2;            // [2] fused SiLU: lane-quarter exchange of column block 0 / 1
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + CF::kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + CF::kOffMisc + 4);
   const int E = prm.seg ? prm.E : 1;
@@ -401,6 +430,10 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&xfull[b], CF::kEpiSetWarps);
       mbar_init(&xempty[b], CF::kEpiSetWarps);
+    }
+    if constexpr (CF::kFuse) {
+      mbar_init(&hx[0], 4);  // the four warps (lane quarters) of a 64-column block
+      mbar_init(&hx[1], 4);
     }
     *s_abort = 0;
     mbar_fence_init();
@@ -454,16 +487,18 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
   // experts, a chain of dependent shared-memory loads that cost each role ~1500 cycles per tile
   // under load); every role then reads a tile with one 16-byte load.
   const int S = SPLIT ? prm.splits : 1;  // 1 folds the split arithmetic away
-  Sched sch{s_prefix, s_start, nullptr, E, NMAX, nblk, S, G / gps, gps};
-  const int n_items = s_prefix[E] * nblk * S;
-  const int n_mine = n_items > static_cast<int>(blockIdx.x)
-                         ? (n_items - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                               static_cast<int>(gridDim.x)
-                         : 0;
+  Sched sch{s_prefix, s_start, nullptr, E, NMAX, nblk, S, G / gps, gps, CF::kFuse ? 1 : 0};
+  // units the CTAs stride over: tiles (x K splits), or gate/up tile pairs
+  const int n_units = s_prefix[E] * nblk * S / (CF::kFuse ? 2 : 1);
+  const int n_mine_units = n_units > static_cast<int>(blockIdx.x)
+                               ? (n_units - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                                     static_cast<int>(gridDim.x)
+                               : 0;
+  const int n_mine = n_mine_units * (CF::kFuse ? 2 : 1);  // this CTA's tiles
   if (n_mine <= prm.tile_cap) {
     for (int i = threadIdx.x; i < n_mine; i += blockDim.x) {
       int e, nb, row0, rows;
-      sch.decode(static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x), e, nb, row0, rows);
+      sch.decode(sch.item_of(i), e, nb, row0, rows);
       s_tiles[i] = make_int4(e, nb, row0, rows);
     }
     sch.tiles = s_tiles;
@@ -485,7 +520,8 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
         const uint64_t pol_w = l2_policy_evict_first();
         const uint32_t w_bytes = gps * CF::kWpkBytes;
         uint32_t st = 0;
-        for (int item = blockIdx.x, it = 0; item < n_items; item += gridDim.x, ++it) {
+        for (int it = 0; it < n_mine; ++it) {
+          const int item = sch.item_of(it);
           int e, nb, row0, rows;
           sch.tile(it, item, e, nb, row0, rows);
           int g_beg, g_end;
@@ -505,7 +541,8 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
         const uint32_t t_bytes = gps * CF::kTokBytes;
         const uint32_t sc_bytes = gps * (2 * NMAX * 4 + kBM * 4);
         uint32_t st = 0;
-        for (int item = blockIdx.x, it = 0; item < n_items; item += gridDim.x, ++it) {
+        for (int it = 0; it < n_mine; ++it) {
+          const int item = sch.item_of(it);
           int e, nb, row0, rows;
           sch.tile(it, item, e, nb, row0, rows);
           const int r4 = row0 & ~3;
@@ -536,7 +573,8 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
         uint32_t st = 0;
         // the next tile's entry is loaded a tile ahead: a tile change costs the MMA issue no load latency
         int4 nxt = sch.tiles && n_mine > 0 ? sch.tiles[0] : make_int4(0, 0, 0, 0);
-        for (int item = blockIdx.x, it = 0; item < n_items; item += gridDim.x, ++it) {
+        for (int it = 0; it < n_mine; ++it) {
+          const int item = sch.item_of(it);
           int e, nb, row0, rows;
           if (sch.tiles) {
             row0 = nxt.z;
@@ -598,7 +636,8 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
     const int cset = (warp - kWarpConv0) / kConvWarps;
     const int r = q4 * 32 + lane;
     uint32_t st = 0;
-    for (int item = blockIdx.x, it = 0; item < n_items; item += gridDim.x, ++it) {
+    for (int it = 0; it < n_mine; ++it) {
+          const int item = sch.item_of(it);
       int g_beg, g_end;
       sch.krange(item, g_beg, g_end);
       for (int g0 = g_beg; g0 < g_end; g0 += gps, ++st) {
@@ -696,7 +735,9 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
       const int cq = 2 * (lane & 3);
       const uint32_t t_lane = static_cast<uint32_t>(q4 * 32) << 16;
       uint32_t st = 0;
-      for (int item = blockIdx.x, it = 0; item < n_items; item += gridDim.x, ++it) {
+      uint32_t hx_phase = 0;  // fused SiLU: completed exchanges of this warp's column block
+      for (int it = 0; it < n_mine; ++it) {
+          const int item = sch.item_of(it);
         int e, nb, row0, rows;
         sch.tile(it, item, e, nb, row0, rows);
         const int r4 = row0 & ~3;
@@ -781,6 +822,154 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
             mbar_arrive(&sempty[ss]);
           }
         }
+        if constexpr (CF::kFuse) {
+          // SiLU-and-Mul with FP8 requantisation fused into the w13 epilogue: tile `it` of a gate / up pair.
+          // The gate tile's values, rounded to bf16 as the unfused path stores them, go to the gate
+          // scratch; the same threads read them back in the up tile and form h = silu(gate) * up, the
+          // amax and the E4M3 code sum of each token's 128 h-columns (own 4 rows, the 8 lanes of the
+          // lane quarter by shuffles, the 4 quarters through shared memory), the codes, the scale and the
+          // correction, with the arithmetic of the SiLU-and-Mul kernel (the same bits).
+          const int np = nblk >> 1;
+          const int I = prm.N >> 1;
+          if (c0 >= need) continue;  // no row of this chunk in the warp's columns (the whole 64-column block)
+          if (nb < np) {  // gate tile
+#pragma unroll
+            for (int rho = 0; rho < 4; ++rho)
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                float a[2];
+                asm("mov.b64 {%0, %1}, %2;" : "=f"(a[0]), "=f"(a[1]) : "l"(acc2[0][rho][v]));
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                  const int t = c0 + 8 * v + cq + q;
+                  if (t < lo || t >= need) continue;
+                  prm.gate[static_cast<int64_t>(r4 + t) * I + nb * kBM + rq + 8 * rho] = float_to_bf16_bits(a[q]);
+                }
+              }
+            continue;
+          }
+          const int gI = nb - np;  // h-group of the up block
+          const int cb = c0 >> 6;  // column block: warps 0-3 (columns 0-63) or 4-7 (64-127)
+          uint8_t* stage = smem + CF::kOffFuse;                                               // [NMAX][kStageRow]
+          float* xmax = reinterpret_cast<float*>(smem + CF::kOffFuse + NMAX * CF::kStageRow);  // [4][NMAX]
+          int* xsum = reinterpret_cast<int*>(xmax + 4 * NMAX);                        // [4][NMAX]
+          float hv[4][8][2];
+          {
+            uint16_t gv[4][8][2];
+#pragma unroll
+            for (int rho = 0; rho < 4; ++rho)
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                  const int t = c0 + 8 * v + cq + q;
+                  gv[rho][v][q] = (t >= lo && t < need)
+                                      ? prm.gate[static_cast<int64_t>(r4 + t) * I + gI * kBM + rq + 8 * rho]
+                                      : uint16_t(0);
+                }
+#pragma unroll
+            for (int rho = 0; rho < 4; ++rho)
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                float a[2];
+                asm("mov.b64 {%0, %1}, %2;" : "=f"(a[0]), "=f"(a[1]) : "l"(acc2[0][rho][v]));
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                  hv[rho][v][q] = silu_mul(bf16_bits_to_float(gv[rho][v][q]),
+                                           bf16_bits_to_float(float_to_bf16_bits(a[q])));
+              }
+          }
+          // amax of each token column over its 128 h-columns
+          float m[8][2];
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              float x = fmaxf(fmaxf(fabsf(hv[0][v][q]), fabsf(hv[1][v][q])), fmaxf(fabsf(hv[2][v][q]), fabsf(hv[3][v][q])));
+#pragma unroll
+              for (int o = 4; o < 32; o <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+              m[v][q] = x;
+            }
+          if ((lane >> 2) == 0) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) *reinterpret_cast<float2*>(xmax + q4 * NMAX + c0 + 8 * v + cq) = make_float2(m[v][0], m[v][1]);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&hx[cb]);
+          if (__any_sync(0xffffffffu, !wait_bar(&hx[cb], hx_phase & 1, s_abort))) goto done;
+          ++hx_phase;
+          float sc[8][2], rc[8][2];
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            float2 x = *reinterpret_cast<const float2*>(xmax + c0 + 8 * v + cq);
+#pragma unroll
+            for (int qq = 1; qq < 4; ++qq) {
+              const float2 y = *reinterpret_cast<const float2*>(xmax + qq * NMAX + c0 + 8 * v + cq);
+              x.x = fmaxf(x.x, y.x);
+              x.y = fmaxf(x.y, y.y);
+            }
+            sc[v][0] = __fdiv_rn(fmaxf(x.x, 1e-12f), 448.0f);
+            sc[v][1] = __fdiv_rn(fmaxf(x.y, 1e-12f), 448.0f);
+            rc[v][0] = __frcp_rn(sc[v][0]);
+            rc[v][1] = __frcp_rn(sc[v][1]);
+          }
+          // codes (staged as token rows) and each token's exact code sum in units of 2^-9
+          int un[8][2];
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+            for (int rho = 0; rho < 4; ++rho) {
+              const uint16_t c2 = e4m3x2(div_by_scale(hv[rho][v][0], sc[v][0], rc[v][0]),
+                                         div_by_scale(hv[rho][v][1], sc[v][1], rc[v][1]));
+              const int t = c0 + 8 * v + cq;
+              stage[t * CF::kStageRow + rq + 8 * rho] = static_cast<uint8_t>(c2 & 0xFF);
+              stage[(t + 1) * CF::kStageRow + rq + 8 * rho] = static_cast<uint8_t>(c2 >> 8);
+              uint32_t h2;
+              asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c2));
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+              s0 += f.x;
+              s1 += f.y;
+            }
+            un[v][0] = __float2int_rn(s0 * 512.0f);
+            un[v][1] = __float2int_rn(s1 * 512.0f);
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+#pragma unroll
+              for (int o = 4; o < 32; o <<= 1) un[v][q] += __shfl_xor_sync(0xffffffffu, un[v][q], o);
+          }
+          if ((lane >> 2) == 0) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) *reinterpret_cast<int2*>(xsum + q4 * NMAX + c0 + 8 * v + cq) = make_int2(un[v][0], un[v][1]);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&hx[cb]);
+          if (__any_sync(0xffffffffu, !wait_bar(&hx[cb], hx_phase & 1, s_abort))) goto done;
+          ++hx_phase;
+          if (q4 == 0 && (lane >> 2) == 0) {  // the scale and correction of each token
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+#pragma unroll
+              for (int q = 0; q < 2; ++q) {
+                const int t = c0 + 8 * v + cq + q;
+                if (t < lo || t >= need) continue;
+                int u = 0;
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) u += xsum[qq * NMAX + t];
+                prm.hs[gI * prm.h_ld + r4 + t] = sc[v][q];
+                if (prm.hc) prm.hc[gI * prm.h_ld + r4 + t] = corr_from_units(u, sc[v][q]);
+              }
+          }
+          // each warp of the column block writes 16 of its 64 token rows of codes, 16 bytes per lane
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int t = c0 + q4 * 16 + 4 * k + (lane >> 3);
+            if (t < lo || t >= need) continue;
+            const uint4 w = *reinterpret_cast<const uint4*>(stage + t * CF::kStageRow + (lane & 7) * 16);
+            *reinterpret_cast<uint4*>(prm.hq + static_cast<int64_t>(r4 + t) * I + gI * kBM + (lane & 7) * 16) = w;
+          }
+          continue;
+        }
 #pragma unroll
         for (int b = 0; b < NB; ++b)
 #pragma unroll
@@ -815,7 +1004,8 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
       const uint32_t t_lane = static_cast<uint32_t>(q4 * 32) << 16;
       constexpr int CH = NHALF < 16 ? 8 : 16;  // columns per tensor-memory load
       uint32_t st = 0, tile = 0;
-      for (int item = blockIdx.x, it = 0; item < n_items; item += gridDim.x, ++tile, ++it) {
+      for (int it = 0; it < n_mine; ++it, ++tile) {
+        const int item = sch.item_of(it);
         int e, nb, row0, rows;
         sch.tile(it, item, e, nb, row0, rows);
         const int r4 = row0 & ~3;
@@ -1039,10 +1229,19 @@ int plan_splits(int64_t M, int64_t N, int64_t K, int sms) {
   return best;
 }
 
+// Outputs of the fused SiLU-and-Mul requantisation (a configuration with kFuse).
+struct FuseOut {
+  uint16_t* gate;  // [M][N/2] bf16 scratch
+  uint8_t* hq;
+  float* hs;
+  float* hc;
+  int64_t h_ld;
+};
+
 template <class CF>
 int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, const uint8_t* B, const float* b_s,
            const int64_t* seg, int64_t E, int64_t N, int64_t K, int64_t M, uint16_t* C, float* partial, int splits,
-           cudaStream_t st, int min_rows = 1, int max_rows = 0x7fffffff) {
+           cudaStream_t st, int min_rows = 1, int max_rows = 0x7fffffff, const FuseOut* fo = nullptr) {
   const int64_t G = K / kGroup;
   const int gps = stage_groups<CF>(K);
   CUtensorMap tA, tAS, tAC, tB, tBS;
@@ -1109,11 +1308,17 @@ int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, c
   p.splits = splits;
   p.min_rows = min_rows;
   p.max_rows = max_rows;
+  p.gate = fo ? fo->gate : nullptr;
+  p.hq = fo ? fo->hq : nullptr;
+  p.hs = fo ? fo->hs : nullptr;
+  p.hc = fo ? fo->hc : nullptr;
+  p.h_ld = fo ? fo->h_ld : 0;
   // tile list: an expert's chunks sit on the NMAX grid from its first row rounded down to 4, so it
   // has at most (3 + rows) / NMAX + 1 of them; tiles = chunks x 128-row blocks x K splits
   const int Ed = seg ? static_cast<int>(E) : 1;
   const int64_t chunks = seg ? (3 * E + M) / CF::NMAX + E + 1 : (M + CF::NMAX - 1) / CF::NMAX + 1;
-  const int64_t per_cta = ceil_div(chunks * (N / kBM) * std::max(splits, 1), num_sms());
+  const int64_t per_cta = CF::kFuse ? 2 * ceil_div(chunks * (N / kBM) / 2, num_sms())
+                                   : ceil_div(chunks * (N / kBM) * std::max(splits, 1), num_sms());
   const int64_t room = (kMaxDynSmem - CF::smem_bytes(Ed, 0)) / 16;
   p.tile_cap = static_cast<int>(std::max<int64_t>(0, std::min(per_cta, room)));
   return launch_pdl("w4a8_gemm_kernel", splits > 1 ? w4a8_gemm_kernel<CF, true> : w4a8_gemm_kernel<CF, false>,
@@ -1133,6 +1338,9 @@ using CfgDecodeLongK = Cfg<16, 4, 5, 4, 6, 2, 3, true, 2, 4, 4, 1>;
 // converted weights go to shared memory (prefill w13 4.378 -> 4.320 ms, w2 2.589 -> 2.504 ms against
 // one group per stage with the weights in tensor memory)
 using CfgPrefill = Cfg<128, 2, 4, 2, 4, 2, 2, false, 2, 2, 8, 1>;
+// the same with the SiLU-and-Mul requantisation fused into the epilogue (w13); one weight stage fewer
+// leaves shared memory for the staged codes
+using CfgPrefillSilu = Cfg<128, 2, 3, 2, 4, 2, 2, false, 2, 2, 8, 1, true>;
 
 // C[m][n] = bf16(sum over s of partial[s][m][n]), four columns per thread.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ partial,
@@ -1287,11 +1495,63 @@ int gemm_common(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_
                     st, static_cast<const float*>(partial), C, MN, S);
 }
 
+// The w13 GEMM followed by SiLU-and-Mul with FP8 requantisation.  When the plan takes the wide tiles only
+// (and a tile has at least two stages), the requantisation runs in the GEMM's epilogue and Y13 is never
+// written (the gate half passes through the workspace as bf16, read back by the threads that wrote it);
+// otherwise the GEMM writes Y13 [M][2I] into the workspace and the SiLU-and-Mul kernel reads it.  Both give
+// the same bits: the fused epilogue rounds gate and up to bf16 and uses the kernel's arithmetic.
+int gemm_silu(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, const uint8_t* B,
+              const float* b_s, const int64_t* seg, int64_t E, int64_t I, int64_t K, int64_t M, uint8_t* q, float* hs,
+              float* hc, int64_t h_ld, void* ws, size_t ws_bytes, void* stream, bool allow_fuse) {
+  W4A8_REQUIRE(seg != nullptr, "seg_indptr is null");
+  W4A8_REQUIRE(I > 0 && I % kGroup == 0, "I=%lld must be a positive multiple of 128", (long long)I);
+  W4A8_REQUIRE(K > 0 && K % kGroup == 0, "K=%lld must be a positive multiple of 128", (long long)K);
+  W4A8_REQUIRE(M >= 0 && M < (1ll << 31), "M=%lld out of range", (long long)M);
+  W4A8_REQUIRE(h_ld >= M && h_ld % 4 == 0 && h_ld > 0, "h_scale_ld=%lld must be >= M and a multiple of 4",
+               (long long)h_ld);
+  W4A8_REQUIRE(a_ld >= M && a_ld % 4 == 0 && a_ld > 0, "a_scale_ld=%lld must be >= M and a multiple of 4",
+               (long long)a_ld);
+  W4A8_REQUIRE(q && hs, "null pointer");
+  W4A8_REQUIRE(aligned16(q) && (reinterpret_cast<uintptr_t>(hs) & 3) == 0 && (reinterpret_cast<uintptr_t>(hc) & 3) == 0,
+               "q must be 16-byte, h_scales and h_gcorr 4-byte aligned");
+  const size_t y_bytes = (static_cast<size_t>(M) * 2 * I * 2 + 255) & ~size_t(255);
+  const size_t need = y_bytes + (a_c ? 0 : static_cast<size_t>(K / kGroup) * a_ld * sizeof(float));
+  W4A8_REQUIRE(ws != nullptr && ws_bytes >= need && aligned16(ws),
+               "workspace of %zu bytes (16-byte aligned) required for this call, got %zu", need, ws_bytes);
+  if (M == 0) return W4A8_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int rc;
+  if (!a_c) {
+    float* corr = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + y_bytes);
+    if ((rc = launch_gcorr(A, M, K, a_s, a_ld, corr, st))) return rc;
+    a_c = corr;
+  }
+  int theta = 0;
+  const int64_t G = K / kGroup;
+  if (allow_fuse && plan_grouped(M, E, K, &theta) == kPlanWide && G / stage_groups<CfgPrefillSilu>(K) >= 2) {
+    W4A8_REQUIRE(E >= 1 && E <= kMaxExperts && E * 2 * I < (1ll << 31), "E=%lld out of range", (long long)E);
+    W4A8_REQUIRE(A && a_s && B && b_s && aligned16(A) && aligned16(a_s) && aligned16(a_c) && aligned16(B) &&
+                     aligned16(b_s),
+                 "GEMM operands must be non-null and 16-byte aligned");
+    const FuseOut fo{static_cast<uint16_t*>(ws), q, hs, hc, h_ld};
+    return launch<CfgPrefillSilu>(A, a_s, a_c, a_ld, B, b_s, seg, E, 2 * I, K, M, nullptr, nullptr, 1, st, 1,
+                                  0x7fffffff, &fo);
+  }
+  uint16_t* y13 = static_cast<uint16_t*>(ws);
+  if ((rc = gemm_common(A, a_s, a_c, a_ld, B, b_s, seg, E, 2 * I, K, M, y13, nullptr, 0, stream))) return rc;
+  return silu_mul_requant(y13, M, I, q, hs, hc, h_ld, stream);
+}
+
 }  // namespace
 
 size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   const int S = linear_splits(M, N, K);
   return S > 1 ? static_cast<size_t>(S) * M * N * sizeof(float) : 0;
+}
+
+size_t gemm_silu_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || K <= 0 || K % kGroup) return 0;
+  return ((static_cast<size_t>(M) * N * 2 + 255) & ~size_t(255)) + gemm_workspace_bytes(M, N, K, false);
 }
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, bool dense) {
@@ -1310,6 +1570,25 @@ extern "C" int w4a8_grouped_gemm(const uint8_t* A, const float* a_scales, const 
   W4A8_REQUIRE(seg_indptr != nullptr, "seg_indptr is null");
   return w4a8::gemm_common(A, a_scales, a_gcorr, a_scale_ld, B_prepacked, b_scales, seg_indptr, E, N, K, M_total, C,
                            ws, ws_bytes, stream);
+}
+
+extern "C" int w4a8_grouped_gemm_silu(const uint8_t* A, const float* a_scales, const float* a_gcorr,
+                                      int64_t a_scale_ld, const uint8_t* B_prepacked, const float* b_scales,
+                                      const int64_t* seg_indptr, int64_t E, int64_t I, int64_t K, int64_t M_total,
+                                      uint8_t* q, float* h_scales, float* h_gcorr, int64_t h_scale_ld, void* ws,
+                                      size_t ws_bytes, void* stream) {
+  return w4a8::gemm_silu(A, a_scales, a_gcorr, a_scale_ld, B_prepacked, b_scales, seg_indptr, E, I, K, M_total, q,
+                         h_scales, h_gcorr, h_scale_ld, ws, ws_bytes, stream, true);
+}
+
+// The same entry point with the fusion switched off (the GEMM then the SiLU-and-Mul kernel): for tests.
+extern "C" int w4a8_grouped_gemm_silu_unfused(const uint8_t* A, const float* a_scales, const float* a_gcorr,
+                                              int64_t a_scale_ld, const uint8_t* B_prepacked, const float* b_scales,
+                                              const int64_t* seg_indptr, int64_t E, int64_t I, int64_t K,
+                                              int64_t M_total, uint8_t* q, float* h_scales, float* h_gcorr,
+                                              int64_t h_scale_ld, void* ws, size_t ws_bytes, void* stream) {
+  return w4a8::gemm_silu(A, a_scales, a_gcorr, a_scale_ld, B_prepacked, b_scales, seg_indptr, E, I, K, M_total, q,
+                         h_scales, h_gcorr, h_scale_ld, ws, ws_bytes, stream, false);
 }
 
 extern "C" int w4a8_linear(const uint8_t* A, const float* a_scales, const float* a_gcorr, int64_t a_scale_ld,
