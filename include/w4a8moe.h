@@ -77,7 +77,9 @@ int w4a8_abi_version(void);
  * (synchronises the device).  Bit 0 (1): a kernel's bounded wait on an
  * mbarrier gave up (W4A8_ERR_TIMEOUT) and that kernel's outputs are invalid.
  * Bit 1 (2): a routed expert id or an expert_map entry was out of range and
- * those pairs were left out.  For tests and diagnostics, not for the hot path.
+ * those pairs were left out.  Bit 2 (4): after such a give-up, waiting for
+ * the GEMM's own in-flight MMAs also ran out of time.  For tests and
+ * diagnostics, not for the hot path.
  */
 int w4a8_device_error(void);
 
@@ -310,6 +312,15 @@ int w4a8_grouped_gemm_plan(int64_t M_total, int64_t E, int64_t K, int* theta);
  * 128-row weight block, and its expectation over Poisson(mean_rows) rows. */
 double w4a8_tile_cost(int wide, int64_t rows);
 double w4a8_expected_tile_cost(int wide, double mean_rows);
+
+/*
+ * Test of the bounded waits: one thread waits, with the GEMMs' wait routine and a limit of limit_ns
+ * (at most 2e9), on an mbarrier that nothing completes.  The wait gives up, sets *gave_up (device int)
+ * to 1 and raises bit 0 of the device error word, as a GEMM wait that times out does (the GEMM then
+ * lets its in-flight MMAs finish, bit 2 if that wait itself times out, and returns early; its outputs
+ * are invalid).  No TMA or MMA is involved.  There is no counterpart of this call in the method.
+ */
+int w4a8_test_wait_timeout(uint64_t limit_ns, int* gave_up, void* stream);
 
 /* Operation ids for w4a8_workspace_bytes. */
 #define W4A8_OP_PERMUTE 1

@@ -222,3 +222,26 @@ def test_quant_scatter_equals_gather(lib, T, K, k, drop):
     assert np.array_equal(sq[:PL].cpu().numpy(), rq[src])
     assert np.array_equal(ss[:, :PL].cpu().numpy().T, rsc[src])
     assert bool((sq[PL:] == 0).all())
+
+
+def test_bounded_wait_gives_up_and_reports(lib):
+    # a wait that nothing completes, with the GEMMs' bounded-wait routine and a 1 ms limit: it gives up,
+    # the device error word carries the timeout bit (once: reading clears it), and the next GEMM is correct
+    import ctypes
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert lib.load().w4a8_test_wait_timeout(1_000_000, ctypes.c_void_p(flag.data_ptr()), st) == 0
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 1
+    assert lib.device_error() == 1
+    assert lib.device_error() == 0
+    rng = np.random.default_rng(3)
+    M, N, K = 300, 256, 1024
+    xb = inputs.to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    aq, a_s, a_c = lib.fp8_quant_per_token_group(bf16_from_bits(xb))
+    packed = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    ws = rng.uniform(0.005, 0.02, size=(K // 128, N)).astype(np.float32)
+    got = lib.w4a8_linear(aq, a_s, a_c, lib.w4a8_prepack_weights(to_dev(packed)), to_dev(ws))
+    ref = oracle.linear(aq.cpu().numpy(), scales_from_gpu_layout(a_s, M), oracle.unpack_int4(packed), ws.T)
+    assert rel_fro(got.float().cpu().numpy().astype(np.float64), ref) <= 1e-3
+    assert lib.device_error() == 0

@@ -84,8 +84,9 @@ int launch_gcorr(const uint8_t* A, int64_t M, int64_t K, const float* a_s, int64
 size_t permute_ws_bytes(int64_t P, int64_t E);
 
 // Device error word: bit 0 = a bounded mbarrier wait timed out, bit 1 = an
-// expert id was out of range.  Each translation unit that can raise one
-// registers a reader with api.cu.
+// expert id was out of range, bit 2 = after a time-out, waiting for a GEMM's own
+// in-flight MMAs ran out of time too.  Each translation unit that can
+// raise one registers a reader with api.cu.
 typedef int (*device_error_reader)(void);
 void register_device_error_reader(device_error_reader f);
 

@@ -125,7 +125,7 @@ struct Cfg {
   static constexpr int kStageRow = 144;  // staged code row: 128 B + 16 B of padding (byte stores spread over banks)
   static constexpr int kFuseBytes = FUSE_ ? NMAX * kStageRow + 2 * 4 * NMAX * 4 : 0;
   static constexpr int kOffBar = kOffFuse + kFuseBytes;
-  static constexpr int kNumBars = 2 * STAGES + 2 * TSTAGES + 2 * SSTAGES + 2 * ABUF + 2 * NP + 4 + (FUSE_ ? 2 : 0);
+  static constexpr int kNumBars = 2 * STAGES + 2 * TSTAGES + 2 * SSTAGES + 2 * ABUF + 2 * NP + 4 + (FUSE_ ? 2 : 0) + 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffSched = kOffMisc + 64;
   // schedule: [E+1] chunk prefix, [E+1] row starts, then (16-byte aligned) [cap] int4 tiles of this CTA
@@ -162,6 +162,7 @@ struct Cfg {
   // waiting on it is never two phases behind.
   static constexpr bool kMmaByStage = GPS_ == 1 && MMAS_ > 1;
   static constexpr int kMmaCommits = kMmaByStage ? 1 : MMAS_;
+  static_assert(MMAS_ >= 1 && MMAS_ <= 4, "one to four MMA-issuing warps (one drain barrier each)");
   static_assert(!kMmaByStage || (TSTAGES_ % MMAS_ == 0 && ABUF_ % MMAS_ == 0),
                 "stage-wise MMA warps: token and A ring depths must be multiples of the MMA warps");
   // Registers a thread gets at launch (the block's share of the 64 K register file, in steps of 8), and the
@@ -300,20 +301,62 @@ struct Sched {
   }
 };
 
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+// Waits for the phase of `bar` with the given parity, at most kTimeoutNs: on expiry it raises the CTA's
+// abort flag and sets bit 0 of the device error word; it also gives up when another role has raised the
+// flag.  Returns whether the phase completed.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         uint64_t limit_ns = kTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 0;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 127u) == 127u) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kTimeoutNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(&g_gemm_error, 1u);
         return false;
       }
     }
   }
+}
+
+// Waits (at most kTimeoutNs, whatever the abort flag) for an asynchronous operation this thread issued:
+// after an abort the MMA-issuing threads let their MMAs finish, so that none writes tensor memory after
+// the CTA has released it.  (On a normal exit the epilogue has waited for every MMA already.)  On expiry
+// sets bit 2 of the error word.
+__device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kTimeoutNs) {
+      atomicOr(&g_gemm_error, 4u);
+      return;
+    }
+  }
+}
+
+// An MMA-issuing thread after an abort: every MMA it issued has completed (a commit arrives once they have).
+// (TMA loads already issued are not waited for: with a drain of the two producers' rings as well, the
+// 16-row decode configuration measured 4 % slower, 0.620 -> 0.645 ms for the w13 launch.)
+__device__ __forceinline__ void drain_mma(uint64_t* bar) {
+  mma_commit(bar);
+  drain_bar(bar, 0);
+}
+
+// A wait that nothing completes: thread 0 waits on a fresh mbarrier with the GEMM's bounded wait and a
+// limit of limit_ns.  The wait gives up, raising the device error word as a timed-out GEMM wait does;
+// *gave_up records it.  Lets a test run the timeout path without any TMA or MMA in flight.
+__global__ void wait_timeout_probe_kernel(uint64_t limit_ns, int* gave_up) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) *gave_up = wait_bar(&bar, 0, &abort_flag, limit_ns) ? 0 : 1;
 }
 
 template <int NCOL>
@@ -391,6 +434,7 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
   uint64_t* xfull = pempty + NP;        // [2] epilogue set 1 -> set 0 hand-over slot written
   uint64_t* xempty = xfull + 2;         // [2] hand-over slot read
   uint64_t* hx = xempty + 2;            // [2] fused SiLU: lane-quarter exchange of column block 0 / 1
+  uint64_t* mdrain = hx + 2;            // [4] per MMA warp: its last MMAs complete (on leaving)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + CF::kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + CF::kOffMisc + 4);
   const int E = prm.seg ? prm.E : 1;
@@ -435,6 +479,7 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
       mbar_init(&hx[0], 4);  // the four warps (lane quarters) of a 64-column block
       mbar_init(&hx[1], 4);
     }
+    for (int m = 0; m < 4; ++m) mbar_init(&mdrain[m], 1);
     *s_abort = 0;
     mbar_fence_init();
   }
@@ -601,7 +646,7 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
             const bool ok = mbar_test3(&tfull[ts_], tph, &mready[a], aph, &pempty[pslot], pph ^ 1) ||
                             (wait_bar(&tfull[ts_], tph, s_abort) && wait_bar(&mready[a], aph, s_abort) &&
                              wait_bar(&pempty[pslot], pph ^ 1, s_abort));
-            if (!ok) goto done;
+            if (!ok) goto m_drain;
             tc_fence_after();
 #pragma unroll
             for (int j = 0; j < GPS; ++j) {
@@ -627,6 +672,8 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
             mma_commit(&tempty[ts_]);
           }
         }
+      m_drain:  // after an abort, the MMAs this thread issued complete before the CTA releases tensor memory
+        if (*s_abort) drain_mma(&mdrain[mset]);
       }
     }
   } else if (warp < kWarpEpi0) {
@@ -1599,6 +1646,14 @@ extern "C" int w4a8_linear(const uint8_t* A, const float* a_scales, const float*
 }
 
 extern "C" int w4a8_linear_split_k(int64_t M, int64_t N, int64_t K) { return w4a8::linear_splits(M, N, K); }
+
+extern "C" int w4a8_test_wait_timeout(uint64_t limit_ns, int* gave_up, void* stream) {
+  using namespace w4a8;
+  W4A8_REQUIRE(gave_up != nullptr && (reinterpret_cast<uintptr_t>(gave_up) & 3) == 0, "gave_up must be an int");
+  W4A8_REQUIRE(limit_ns > 0 && limit_ns <= kTimeoutNs, "limit_ns must be in (0, 2e9]");
+  wait_timeout_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns, gave_up);
+  return check_launch("wait_timeout_probe_kernel");
+}
 
 extern "C" double w4a8_tile_cost(int wide, int64_t rows) { return w4a8::tile_cost(wide, rows); }
 
