@@ -683,9 +683,9 @@ def run_linear(args, cfg, dev, world, rank, peaks, peak_src):
     ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     sp = torch.cuda.current_stream(dev).cuda_stream
 
-    def step(i):
+    def step(i, stream=sp):
         return lib.w4a8_linear(aq.data_ptr(), a_s.data_ptr(), a_c.data_ptr(), a_s.shape[1], Ws[i % copies].data_ptr(),
-                               Ss[i % copies].data_ptr(), M, N, K, C.data_ptr(), ws.data_ptr(), need, sp)
+                               Ss[i % copies].data_ptr(), M, N, K, C.data_ptr(), ws.data_ptr(), need, stream)
 
     for i in range(args.warmup):
         step(i)
@@ -693,7 +693,7 @@ def run_linear(args, cfg, dev, world, rank, peaks, peak_src):
     Kst = args.steps
     # events only around the K calls: the calls are launched back to back, as a model would, so a
     # call's launch and prologue overlap the previous call (programmatic dependent launch)
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     with clock_sampler(dev) as clk:
         evs[0].record()
         for i in range(Kst):
@@ -702,7 +702,23 @@ def run_linear(args, cfg, dev, world, rank, peaks, peak_src):
                 raise RuntimeError(lib.w4a8_last_error().decode())
         evs[1].record()
         torch.cuda.synchronize(dev)
-    ms = evs[0].elapsed_time(evs[-1])
+    eager_ms = evs[0].elapsed_time(evs[1])
+    # The same K calls captured once in a CUDA graph and replayed: a call of a few microseconds is then
+    # timed without the host's submission (a Python call per kernel, which a thread switch can stall)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        cs = torch.cuda.current_stream(dev).cuda_stream
+        for i in range(Kst):
+            if step(i, cs):
+                raise RuntimeError(lib.w4a8_last_error().decode())
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    with clock_sampler(dev) as clk:
+        evs[2].record()
+        graph.replay()
+        evs[3].record()
+        torch.cuda.synchronize(dev)
+    ms = evs[2].elapsed_time(evs[3])
     ms_step = ms / Kst
     cnt = linear_counts(M, N, K)
     tf = cnt["flops"] / (ms_step / 1e3) / 1e12
@@ -714,7 +730,10 @@ def run_linear(args, cfg, dev, world, rank, peaks, peak_src):
     res = {"metric": METRIC, "value": round(M / (ms_step / 1e3), 2), "unit": "tokens/s", "n_gpus": world,
            "steps": Kst, "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x int4 -> f32 (bf16 out)", "data": "synthetic",
-           "config": {"workload": workload_desc("linear", cfg), "l2": f"{copies} rotating weight copies"},
+           "config": {"workload": workload_desc("linear", cfg), "l2": f"{copies} rotating weight copies",
+                      "timing": "the K calls replayed from a CUDA graph captured once (eager_ms_per_step: the same "
+                                "calls launched one by one from Python)"},
+           "eager_ms_per_step": round(eager_ms / Kst, 5),
            "tflops": round(tf, 2), "roofline": roof, "gpu_launches": Kst * (2 if m.linear_split_k(M, N, K) > 1 else 1),
            "split_k": m.linear_split_k(M, N, K), "clocks": clk.summary()}
     if rank == 0:
