@@ -322,6 +322,15 @@ double w4a8_expected_tile_cost(int wide, double mean_rows);
  */
 int w4a8_test_wait_timeout(uint64_t limit_ns, int* gave_up, void* stream);
 
+/*
+ * Test of the GEMMs' in-place tile decode: every CTA of a GEMM launch normally decodes its tiles once into
+ * a shared-memory list, and decodes each tile in place (a search over the experts' chunk prefix) only when
+ * the list would not fit, which takes launches of hundreds of thousands of rows.  This call bounds the list
+ * at max_tiles tiles per CTA for the launches that follow, process-wide (0: always decode in place;
+ * negative: no bound, the default).  Results do not depend on it.  Returns W4A8_OK.
+ */
+int w4a8_test_tile_list_limit(int max_tiles);
+
 /* Operation ids for w4a8_workspace_bytes. */
 #define W4A8_OP_PERMUTE 1
 #define W4A8_OP_GROUPED_GEMM 2

@@ -249,3 +249,49 @@ def test_gemm_without_corrections_needs_workspace(lib):
 
 def scale_ld_of(M):
     return max(4, (M + 3) // 4 * 4)
+
+
+def test_in_place_tile_decode_matches_the_tile_list(lib):
+    # Launches too large for the per-CTA shared-memory tile list decode each tile in place instead (a
+    # search over the experts' chunk prefix).  Bounding the list at 0 tiles forces that path on small
+    # shapes: the 16-wide, 128-wide and split plans, the dense split-K Linear and the fused SiLU epilogue
+    # must give the same bits as with the list.
+    clib = lib.load()
+    rng = np.random.default_rng(2024)
+    K = 1024
+    cases = []
+    for counts, N in (([3, 0, 17, 1, 9, 2], 256), ([300, 0, 129, 513], 256), ([40, 3, 200, 0, 1, 77], 128)):
+        E = len(counts)
+        seg = np.concatenate([[0], np.cumsum(counts)])
+        aq, a_s = _acts(rng, int(seg[-1]), K)
+        packed, ws = _weights(rng, E, N, K)
+        cases.append(lambda aq=aq, a_s=a_s, packed=packed, ws=ws, seg=seg: _run_grouped(lib, aq, a_s, packed, ws, seg))
+    aq, a_s = _acts(rng, 1, 8192)
+    packed, ws = _weights(rng, 1, 1024, 8192)
+    assert lib.linear_split_k(1, 1024, 8192) > 1
+    cases.append(lambda: lib.w4a8_linear(to_dev(aq), scales_to_gpu_layout(a_s), None, prepacked(lib, packed[0]),
+                                         to_dev(ws[0])))
+    seg = np.array([0, 300, 300, 557], dtype=np.int64)
+    xq, xs = _acts(rng, 557, K)
+    packed2, ws2 = _weights(rng, 3, 512, K)
+    B2 = prepacked(lib, packed2)
+
+    def fused():
+        q, s, c = lib.w4a8_grouped_gemm_silu(to_dev(xq), scales_to_gpu_layout(xs), None, B2, to_dev(ws2),
+                                             to_dev(seg), fused=True)
+        M = int(seg[-1])  # the scale rows past M are padding the kernels never write
+        return torch.cat([q.flatten(), s[:, :M].contiguous().flatten().view(torch.uint8),
+                          c[:, :M].contiguous().flatten().view(torch.uint8)])
+
+    cases.append(fused)
+    ref = [f().clone() for f in cases]
+    torch.cuda.synchronize()
+    try:
+        assert clib.w4a8_test_tile_list_limit(0) == 0
+        got = [f().clone() for f in cases]
+        torch.cuda.synchronize()
+    finally:
+        clib.w4a8_test_tile_list_limit(-1)
+    assert lib.device_error() == 0
+    for i, (g, r) in enumerate(zip(got, ref)):
+        assert torch.equal(g, r), i

@@ -47,6 +47,7 @@ _SIGS = {
     "w4a8_workspace_bytes": (_c_sz, [_c_int, _c_i64, _c_i64, _c_i64, _c_i64]),
     "w4a8_linear_split_k": (_c_int, [_c_i64, _c_i64, _c_i64]),
     "w4a8_test_wait_timeout": (_c_int, [ctypes.c_uint64, _c_vp, _c_vp]),
+    "w4a8_test_tile_list_limit": (_c_int, [_c_int]),
     "w4a8_grouped_gemm_plan": (_c_int, [_c_i64, _c_i64, _c_i64, ctypes.POINTER(_c_int)]),
     "w4a8_tile_cost": (ctypes.c_double, [_c_int, _c_i64]),
     "w4a8_expected_tile_cost": (ctypes.c_double, [_c_int, ctypes.c_double]),

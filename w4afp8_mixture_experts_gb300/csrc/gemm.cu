@@ -57,6 +57,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <atomic>
 #include <cstring>
 
 #include "common.cuh"
@@ -1279,6 +1280,10 @@ struct FuseOut {
   int64_t h_ld;
 };
 
+// Upper bound on the shared-memory tile list (tiles per CTA), for tests of the in-place tile decode that
+// launches too large for the list fall back to; negative: no bound.
+std::atomic<int> g_tile_cap_limit{-1};
+
 template <class CF>
 int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, const uint8_t* B, const float* b_s,
            const int64_t* seg, int64_t E, int64_t N, int64_t K, int64_t M, uint16_t* C, float* partial, int splits,
@@ -1362,6 +1367,8 @@ int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, c
                                    : ceil_div(chunks * (N / kBM) * std::max(splits, 1), num_sms());
   const int64_t room = (kMaxDynSmem - CF::smem_bytes(Ed, 0)) / 16;
   p.tile_cap = static_cast<int>(std::max<int64_t>(0, std::min(per_cta, room)));
+  const int cap_limit = g_tile_cap_limit.load();
+  if (cap_limit >= 0 && p.tile_cap > cap_limit) p.tile_cap = cap_limit;
   return launch_pdl("w4a8_gemm_kernel", splits > 1 ? w4a8_gemm_kernel<CF, true> : w4a8_gemm_kernel<CF, false>,
                     dim3(num_sms()), dim3(CF::kThreads), CF::smem_bytes(Ed, p.tile_cap), st, tA, tAS,
                     tAC, tB, tBS, p);
@@ -1640,6 +1647,11 @@ extern "C" int w4a8_linear(const uint8_t* A, const float* a_scales, const float*
 }
 
 extern "C" int w4a8_linear_split_k(int64_t M, int64_t N, int64_t K) { return w4a8::linear_splits(M, N, K); }
+
+extern "C" int w4a8_test_tile_list_limit(int max_tiles) {
+  w4a8::g_tile_cap_limit.store(max_tiles < 0 ? -1 : max_tiles);
+  return W4A8_OK;
+}
 
 extern "C" int w4a8_test_wait_timeout(uint64_t limit_ns, int* gave_up, void* stream) {
   using namespace w4a8;
