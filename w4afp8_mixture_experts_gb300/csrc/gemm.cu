@@ -153,7 +153,7 @@ struct Cfg {
   // accumulators need more registers than an even split gives, so these tiles also move registers
   // from the producer/MMA warpgroup and the converters to the epilogue warpgroups.
   static constexpr int kEpiCols = NMAX_ * 4 / (EPIW_ / EPIS_);  // columns per epilogue warp
-  static constexpr bool kEpi16 = NMAX_ >= 64 && EPIS_ == 1 && kEpiCols % 64 == 0;
+  static constexpr bool kEpi16 = NMAX_ >= 64 && EPIS_ == 1 && kEpiCols % 32 == 0;
   static constexpr bool kRegSplit = kEpi16;
   // With one group per stage the MMA warps take whole stages in turn (warp m: stages st % MMAS == m)
   // instead of groups of a stage, and each stage's barriers get one commit.  A token or A slot is
@@ -771,11 +771,11 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
   } else {
     if constexpr (CF::kRegSplit) regs_claim<CF::kRegsEpi>();
     if constexpr (CF::kEpi16) {
-      // 16x256b fragments: thread t of the warp for lane quarter q4 and column block `half` holds,
-      // for each 64-column block b, rows q4*32 + t/4 + 8*rho (rho = 0..3) and columns
-      // c0 + 64*b + 8*v + 2*(t%4) + {0, 1} (v = 0..7): a token scale pair read from shared memory
+      // 16x256b fragments: thread t of the warp for lane quarter q4 and its NHALF columns from c0 holds,
+      // for each 32-column block hb, rows q4*32 + t/4 + 8*rho (rho = 0..3) and columns
+      // c0 + 32*hb + 8*v + 2*(t%4) + {0, 1} (v = 0..3): a token scale pair read from shared memory
       // serves four rows.  Same promotion, same order of groups as the 32x32b path below.
-      constexpr int NB = NHALF / 64;
+      constexpr int NB32 = NHALF / 32;
       const int ew = warp - kWarpEpi0;
       const int q4 = warp & 3;
       const int c0 = (ew >> 2) * NHALF;
@@ -790,14 +790,14 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
         sch.tile(it, item, e, nb, row0, rows);
         const int r4 = row0 & ~3;
         const int lo = row0 - r4;    // columns [lo, lo + rows) of the tile are this chunk's rows
-        const int need = lo + rows;  // 64-column blocks from `need` on are never stored: skipped
-        uint64_t acc2[NB][4][8];
+        const int need = lo + rows;  // 32-column blocks from `need` on are never stored: skipped
+        uint64_t acc2[NB32][4][4];
 #pragma unroll
-        for (int b = 0; b < NB; ++b)
+        for (int hb = 0; hb < NB32; ++hb)
 #pragma unroll
           for (int rho = 0; rho < 4; ++rho)
 #pragma unroll
-            for (int v = 0; v < 8; ++v) acc2[b][rho][v] = 0ull;
+            for (int v = 0; v < 4; ++v) acc2[hb][rho][v] = 0ull;
         int g_beg, g_end;
         sch.krange(item, g_beg, g_end);
         for (int g0 = g_beg; g0 < g_end; g0 += gps, ++st) {
@@ -819,41 +819,38 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
             const float* wsj = wsc + j * kBM + rq;
             const float* ts = tsc + j * NMAX + c0 + cq;
             const float* tc = tcr + j * NMAX + c0 + cq;
+            if (c0 >= need) continue;  // warp-uniform: none of this warp's columns is stored
+            uint64_t ws2[4];
 #pragma unroll
-            for (int b = 0; b < NB; ++b) {
-              if (c0 + 64 * b >= need) continue;  // warp-uniform
-              uint64_t ws2[4];
+            for (int rho = 0; rho < 4; ++rho) {
+              const float w = wsj[8 * rho];
+              asm("mov.b64 %0, {%1, %1};" : "=l"(ws2[rho]) : "f"(w));
+            }
+            // the partials in 32-column blocks, one tensor-memory wait each (reading them in 16-column
+            // chunks, each chunk's read in flight while the previous one is promoted, measured 2 %
+            // slower: a wait per 16 columns)
+            const uint32_t pa = tmem_base + t_lane + (pslot * GPS + j) * NMAX + c0;
 #pragma unroll
-              for (int rho = 0; rho < 4; ++rho) {
-                const float w = wsj[8 * rho];
-                asm("mov.b64 %0, {%1, %1};" : "=l"(ws2[rho]) : "f"(w));
-              }
-              // the block's partials in two 32-column halves, one wait each (reading them in four
-              // 16-column chunks, each chunk's read in flight while the previous one is promoted,
-              // measured 2 % slower: a wait per 16 columns)
-              const uint32_t pa = tmem_base + t_lane + (pslot * GPS + j) * NMAX + c0 + 64 * b;
+            for (int hb = 0; hb < NB32; ++hb) {
+              if (c0 + 32 * hb >= need) continue;  // warp-uniform
+              uint32_t qa[16], qb[16];  // lanes +0 and +16 of the quarter: rows rho = 0, 1 and 2, 3
+              tmem_ld16x256b_x4(pa + 32 * hb, qa);
+              tmem_ld16x256b_x4(pa + 32 * hb + (16u << 16), qb);
+              tmem_wait_ld_pin<16>(qa);
 #pragma unroll
-              for (int hf = 0; hf < 2; ++hf) {
-                uint32_t qa[16], qb[16];  // lanes +0 and +16 of the quarter: rows rho = 0, 1 and 2, 3
-                tmem_ld16x256b_x4(pa + 32 * hf, qa);
-                tmem_ld16x256b_x4(pa + 32 * hf + (16u << 16), qb);
-                tmem_wait_ld_pin<16>(qa);
+              for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(qb[i]));
 #pragma unroll
-                for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(qb[i]));
+              for (int v = 0; v < 4; ++v) {
+                const uint64_t t2 = *reinterpret_cast<const uint64_t*>(ts + 32 * hb + 8 * v);
+                const uint64_t k2 = *reinterpret_cast<const uint64_t*>(tc + 32 * hb + 8 * v);
 #pragma unroll
-                for (int vv = 0; vv < 4; ++vv) {
-                  const int v = 4 * hf + vv;
-                  const uint64_t t2 = *reinterpret_cast<const uint64_t*>(ts + 64 * b + 8 * v);
-                  const uint64_t k2 = *reinterpret_cast<const uint64_t*>(tc + 64 * b + 8 * v);
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
-                  for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int jj = 0; jj < 2; ++jj) {
-                      const uint32_t* cur = h ? qb : qa;
-                      const int i = 4 * vv + 2 * jj;
-                      promote2p(acc2[b][2 * h + jj][v], ws2[2 * h + jj], t2, k2, cur[i], cur[i + 1]);
-                    }
-                }
+                  for (int jj = 0; jj < 2; ++jj) {
+                    const uint32_t* cur = h ? qb : qa;
+                    const int i = 4 * v + 2 * jj;
+                    promote2p(acc2[hb][2 * h + jj][v], ws2[2 * h + jj], t2, k2, cur[i], cur[i + 1]);
+                  }
               }
             }
           }
@@ -880,7 +877,7 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
 #pragma unroll
               for (int v = 0; v < 8; ++v) {
                 float a[2];
-                asm("mov.b64 {%0, %1}, %2;" : "=f"(a[0]), "=f"(a[1]) : "l"(acc2[0][rho][v]));
+                asm("mov.b64 {%0, %1}, %2;" : "=f"(a[0]), "=f"(a[1]) : "l"(acc2[v >> 2][rho][v & 3]));
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                   const int t = c0 + 8 * v + cq + q;
@@ -914,7 +911,7 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
 #pragma unroll
               for (int v = 0; v < 8; ++v) {
                 float a[2];
-                asm("mov.b64 {%0, %1}, %2;" : "=f"(a[0]), "=f"(a[1]) : "l"(acc2[0][rho][v]));
+                asm("mov.b64 {%0, %1}, %2;" : "=f"(a[0]), "=f"(a[1]) : "l"(acc2[v >> 2][rho][v & 3]));
 #pragma unroll
                 for (int q = 0; q < 2; ++q)
                   hv[rho][v][q] = silu_mul(bf16_bits_to_float(gv[rho][v][q]),
@@ -1013,17 +1010,17 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
           continue;
         }
 #pragma unroll
-        for (int b = 0; b < NB; ++b)
+        for (int hb = 0; hb < NB32; ++hb)
 #pragma unroll
           for (int rho = 0; rho < 4; ++rho)
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
+            for (int v = 0; v < 4; ++v) {
               float a[2];
-              asm("mov.b64 {%0, %1}, %2;" : "=f"(a[0]), "=f"(a[1]) : "l"(acc2[b][rho][v]));
+              asm("mov.b64 {%0, %1}, %2;" : "=f"(a[0]), "=f"(a[1]) : "l"(acc2[hb][rho][v]));
               const int n = nb * kBM + rq + 8 * rho;  // output column: weight row of the block
 #pragma unroll
               for (int q = 0; q < 2; ++q) {
-                const int t = c0 + 64 * b + 8 * v + cq + q;  // tile column: token row r4 + t
+                const int t = c0 + 32 * hb + 8 * v + cq + q;  // tile column: token row r4 + t
                 if (t < lo || t >= need) continue;
                 const int64_t m = r4 + t;
                 if (SPLIT)
