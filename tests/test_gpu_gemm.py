@@ -127,6 +127,29 @@ def test_linear_split_k(lib, M, N, K):
     assert lib.device_error() == 0
 
 
+def test_linear_split_k_workspace_contents_do_not_matter(lib):
+    # The partial sums live in the caller's workspace: whatever it held before (bytes of 0xFF, random
+    # bytes, the previous call's partials) the result is the same, bit for bit, and matches the oracle.
+    M, N, K = 1, 1024, 8192
+    assert lib.linear_split_k(M, N, K) > 1
+    rng = np.random.default_rng(9)
+    aq, a_s = _acts(rng, M, K)
+    packed, ws = _weights(rng, 1, N, K)
+    args = (to_dev(aq), scales_to_gpu_layout(a_s), scales_to_gpu_layout(gcorr_of(aq, a_s)), prepacked(lib, packed[0]),
+            to_dev(ws[0]))
+    need = lib.linear_workspace_bytes(M, N, K)
+    buf = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    outs = [lib.w4a8_linear(*args, ws=buf).clone()]
+    buf.copy_(torch.from_numpy(rng.integers(0, 256, need, dtype=np.uint8)))
+    outs.append(lib.w4a8_linear(*args, ws=buf).clone())
+    outs += [lib.w4a8_linear(*args, ws=buf).clone() for _ in range(3)]  # the words of the previous calls
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+    assert all(torch.equal(o, outs[0]) for o in outs[1:])
+    ref = oracle.linear(aq, a_s, oracle.unpack_int4(packed[0]), ws[0].T)
+    assert rel_fro(f64_of_bf16(outs[0]), ref) <= 1e-3
+
+
 def test_linear_split_k_needs_workspace(lib):
     M, N, K = 1, 1024, 8192
     rng = np.random.default_rng(5)

@@ -126,7 +126,16 @@ struct Cfg {
   static constexpr int kStageRow = 144;  // staged code row: 128 B + 16 B of padding (byte stores spread over banks)
   static constexpr int kFuseBytes = FUSE_ ? NMAX * kStageRow + 2 * 4 * NMAX * 4 : 0;
   static constexpr int kOffBar = kOffFuse + kFuseBytes;
-  static constexpr int kNumBars = 2 * STAGES + 2 * TSTAGES + 2 * SSTAGES + 2 * ABUF + 2 * NP + 4 + (FUSE_ ? 2 : 0) + 4;
+  // mbarrier area, in 8-byte slots: the rings, then xfull[2], xempty[2], hx[2] (used by the fused epilogue
+  // only, always laid out) and mdrain[4]; the kernel takes every array's address from these offsets
+  static constexpr int kBarFull = 0, kBarEmpty = kBarFull + STAGES;
+  static constexpr int kBarTfull = kBarEmpty + STAGES, kBarTempty = kBarTfull + TSTAGES;
+  static constexpr int kBarSfull = kBarTempty + TSTAGES, kBarSempty = kBarSfull + SSTAGES;
+  static constexpr int kBarMready = kBarSempty + SSTAGES, kBarMdone = kBarMready + ABUF;
+  static constexpr int kBarPfull = kBarMdone + ABUF, kBarPempty = kBarPfull + NP;
+  static constexpr int kBarXfull = kBarPempty + NP, kBarXempty = kBarXfull + 2;
+  static constexpr int kBarHx = kBarXempty + 2, kBarMdrain = kBarHx + 2;
+  static constexpr int kNumBars = kBarMdrain + 4;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffSched = kOffMisc + 64;
   // schedule: [E+1] chunk prefix, [E+1] row starts, then (16-byte aligned) [cap] int4 tiles of this CTA
@@ -422,20 +431,20 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
   uint8_t* s_sc = smem + CF::kOffSc;    // [SSTAGES] slot: [GPS][NMAX] token scales, [GPS][NMAX] corrections,
                                         //   [GPS][128] weight scales
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + CF::kOffBar);
-  uint64_t* full = bars;                // weight ring
-  uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;     // token ring
-  uint64_t* tempty = tfull + TSTAGES;
-  uint64_t* sfull = tempty + TSTAGES;   // scale ring
-  uint64_t* sempty = sfull + SSTAGES;
-  uint64_t* mready = sempty + SSTAGES;  // [ABUF] converted weights of a stage ready for the MMAs
-  uint64_t* mdone = mready + ABUF;      // [ABUF] MMAs of the stage done: A slot free
-  uint64_t* pfull = mdone + ABUF;       // [NP] MMAs of the stage done: partials ready
-  uint64_t* pempty = pfull + NP;        // [NP] partial slot read by the epilogue
-  uint64_t* xfull = pempty + NP;        // [2] epilogue set 1 -> set 0 hand-over slot written
-  uint64_t* xempty = xfull + 2;         // [2] hand-over slot read
-  uint64_t* hx = xempty + 2;            // [2] fused SiLU: lane-quarter exchange of column block 0 / 1
-  uint64_t* mdrain = hx + 2;            // [4] per MMA warp: its last MMAs complete (on leaving)
+  uint64_t* full = bars + CF::kBarFull;      // weight ring
+  uint64_t* empty = bars + CF::kBarEmpty;
+  uint64_t* tfull = bars + CF::kBarTfull;    // token ring
+  uint64_t* tempty = bars + CF::kBarTempty;
+  uint64_t* sfull = bars + CF::kBarSfull;    // scale ring
+  uint64_t* sempty = bars + CF::kBarSempty;
+  uint64_t* mready = bars + CF::kBarMready;  // [ABUF] converted weights of a stage ready for the MMAs
+  uint64_t* mdone = bars + CF::kBarMdone;    // [ABUF] MMAs of the stage done: A slot free
+  uint64_t* pfull = bars + CF::kBarPfull;    // [NP] MMAs of the stage done: partials ready
+  uint64_t* pempty = bars + CF::kBarPempty;  // [NP] partial slot read by the epilogue
+  uint64_t* xfull = bars + CF::kBarXfull;    // [2] epilogue set 1 -> set 0 hand-over slot written
+  uint64_t* xempty = bars + CF::kBarXempty;  // [2] hand-over slot read
+  uint64_t* hx = bars + CF::kBarHx;          // [2] fused SiLU: lane-quarter exchange of column block 0 / 1
+  uint64_t* mdrain = bars + CF::kBarMdrain;  // [4] per MMA warp: its last MMAs complete (on leaving)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + CF::kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + CF::kOffMisc + 4);
   const int E = prm.seg ? prm.E : 1;
