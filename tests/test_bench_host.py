@@ -245,3 +245,13 @@ def test_oracle_over_host_cores_runs_rounds_together():
     rounds, tokens, cores = bench.oracle_on_host_cores("tiny", cfg, 0, 1, 2, cores=2)
     assert len(rounds) == 2 and tokens == 2 and cores == 2
     assert all(0.0 < r < 60.0 for r in rounds)
+
+
+def test_e2e_copies_and_pipelining_rule():
+    # tiny: 32 KiB in, 2 KiB of logits, 32 KiB out -> copies in order; decode: 0.92 MiB of x + 64 KiB of
+    # logits in, 0.88 MiB out -> overlapped with the layer; prefill likewise
+    assert bench.e2e_bytes(64, 256, 8) == (64 * 256 * 2 + 64 * 8 * 4, 64 * 256 * 2)
+    assert not bench.e2e_pipelined(*bench.e2e_bytes(64, 256, 8))
+    assert bench.e2e_bytes(64, 7168, 256) == (983040, 917504)
+    assert bench.e2e_pipelined(*bench.e2e_bytes(64, 7168, 256))
+    assert bench.e2e_pipelined(*bench.e2e_bytes(8192, 7168, 256))
