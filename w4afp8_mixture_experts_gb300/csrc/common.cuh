@@ -166,6 +166,12 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
 }
 
+// A 2-byte global store that does not allocate in L1 (an output the block never reads back; the next
+// kernel reads it through L2): measured ~0.5 % faster for the 128-token GEMM's tile-end stores.
+__device__ __forceinline__ void st_global_na_u16(uint16_t* p, uint16_t v) {
+  asm volatile("st.global.L1::no_allocate.b16 [%0], %1;" ::"l"(p), "h"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));

@@ -1035,7 +1035,7 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
                 if (SPLIT)
                   prm.partial[(static_cast<int64_t>(item % sch.S) * prm.M + m) * prm.N + n] = a[q];
                 else
-                  prm.C[m * prm.N + n] = float_to_bf16_bits(a[q]);
+                  st_global_na_u16(prm.C + m * prm.N + n, float_to_bf16_bits(a[q]));
               }
             }
       }
