@@ -318,3 +318,30 @@ def test_in_place_tile_decode_matches_the_tile_list(lib):
     assert lib.device_error() == 0
     for i, (g, r) in enumerate(zip(got, ref)):
         assert torch.equal(g, r), i
+
+
+@pytest.mark.parametrize("plan_rows", ["narrow", "split", "wide"])
+def test_grouped_gemm_at_the_expert_limit(lib, plan_rows):
+    # 1024 experts (the largest count the kernels take: the per-CTA chunk prefix and row starts then fill
+    # 8 KB of shared memory and shorten the tile list), most of them empty, the rest with few or many rows
+    rng = np.random.default_rng({"narrow": 1, "split": 2, "wide": 3}[plan_rows])
+    E, N, K = 1024, 128, 256
+    counts = np.zeros(E, dtype=np.int64)
+    used = rng.choice(E, 48, replace=False)
+    if plan_rows == "narrow":
+        counts[used] = rng.integers(1, 20, used.size)
+    elif plan_rows == "split":
+        counts[used] = rng.integers(1, 20, used.size)
+        counts[used[:30]] = rng.integers(150, 400, 30)
+    else:
+        counts[used] = rng.integers(200, 400, used.size)
+    counts[0], counts[E - 1] = 3, 257  # the first and the last expert hold rows
+    seg = np.concatenate([[0], np.cumsum(counts)])
+    M = int(seg[-1])
+    aq, a_s = _acts(rng, M, K)
+    packed, ws = _weights(rng, E, N, K)
+    got = f64_of_bf16(_run_grouped(lib, aq, a_s, packed, ws, seg))
+    ref = _oracle_grouped(aq, a_s, packed, ws, seg)
+    err = rel_fro(got, ref)
+    assert err <= 1e-3, (plan_rows, err)
+    assert lib.device_error() == 0

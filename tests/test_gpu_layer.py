@@ -53,6 +53,7 @@ def _ws_view(ws, off, dtype, shape):
     ("many-experts", dict(T=200, H=512, I=384, E=160, k=6)),
     ("prefill-tiles", dict(T=700, H=256, I=256, E=4, k=2)),
     ("wide-two-stages", dict(T=600, H=512, I=256, E=4, k=2)),
+    ("expert-limit", dict(T=300, H=256, I=128, E=1024, k=8)),  # the largest expert count the layer takes
 ])
 def test_layer_stage_by_stage(lib, name, cfg):
     seed = 3
