@@ -86,3 +86,38 @@ def test_expected_cost_mid_mean(clib):
 def test_plans_of_the_workloads(clib, M, E, K, plan):
     th = ctypes.c_int()
     assert clib.w4a8_grouped_gemm_plan(M, E, K, ctypes.byref(th)) == plan
+
+
+def _plan_splits_by_hand(M, N, K, sms=152):
+    # the dense Linear's K splits as the estimate defines them: 16-wide tiles (4 groups per stage) up to
+    # 32 rows, 128-wide tiles (2 groups per stage) above; S = 1 .. 16 minimising
+    # ceil(items / SMs) * ceil(stages / S) + 2 (S > 1), partials at most a quarter of the weight bytes
+    nmax, gmax = (16, 4) if M <= 32 else (128, 2)
+    G = K // 128
+    gps = 1
+    while gps * 2 <= gmax and G % (gps * 2) == 0:
+        gps *= 2
+    tiles = -(-M // nmax) * (N // 128)
+    if tiles >= sms:
+        return 1
+    stages = G // gps
+    best, best_cost = 1, -(-tiles // sms) * stages
+    for S in range(2, 17):
+        if S > stages or S * M * N * 4 > N * K // 8:
+            break
+        cost = -(-tiles * S // sms) * -(-stages // S) + 2
+        if cost < best_cost:
+            best, best_cost = S, cost
+    return best
+
+
+@pytest.mark.parametrize("N,K", [(24576, 1536), (7168, 16384), (18432, 7168), (7168, 2048), (1024, 8192), (256, 32768)])
+def test_linear_split_plan(clib, N, K):
+    # on a host without a GPU the library plans for the GB300's 152 SMs
+    clib.w4a8_linear_split_k.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
+    for M in (1, 13, 16, 40, 128, 130, 1024, 8192):
+        S = clib.w4a8_linear_split_k(M, N, K)
+        assert S == _plan_splits_by_hand(M, N, K), (M, N, K, S)
+        assert 1 <= S <= 16 and (S == 1 or S * M * N * 4 <= N * K // 8)
+    # the sweep's one split shape family: (7168, 16384) splits 8 ways at M = 1 and 16, twice at 128
+    assert [clib.w4a8_linear_split_k(M, 7168, 16384) for M in (1, 16, 128, 1024)] == [8, 8, 2, 1]
