@@ -822,6 +822,62 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
             ok = wait_bar(&sfull[ss], sph, s_abort) && wait_bar(&pfull[pslot], pph, s_abort);
           if (__any_sync(0xffffffffu, !ok)) goto done;  // warp converged below
           tc_fence_after();
+          if (gps == GPS && need >= c0 + NHALF) {
+            // every 32-column block of every group of the stage is promoted: the next block's
+            // tensor-memory read is issued before the current block is promoted (two buffers), so each
+            // wait covers one read that has been in flight for a block's promotion
+            uint32_t qa0[16], qb0[16], qa1[16], qb1[16];
+            {
+              const uint32_t pa0 = tmem_base + t_lane + (pslot * GPS) * NMAX + c0;
+              tmem_ld16x256b_x4(pa0, qa0);
+              tmem_ld16x256b_x4(pa0 + (16u << 16), qb0);
+              tmem_wait_ld_pin<16>(qa0);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(qb0[i]));
+            }
+            uint64_t ws2[4];
+#pragma unroll
+            for (int u = 0; u < GPS * NB32; ++u) {
+              const int j = u / NB32, hb = u % NB32;
+              uint32_t* ca = (u & 1) ? qa1 : qa0;
+              uint32_t* cb = (u & 1) ? qb1 : qb0;
+              uint32_t* na = (u & 1) ? qa0 : qa1;
+              uint32_t* nbuf = (u & 1) ? qb0 : qb1;
+              if (u + 1 < GPS * NB32) {
+                const int j1 = (u + 1) / NB32, hb1 = (u + 1) % NB32;
+                const uint32_t pa1 = tmem_base + t_lane + (pslot * GPS + j1) * NMAX + c0 + 32 * hb1;
+                tmem_ld16x256b_x4(pa1, na);
+                tmem_ld16x256b_x4(pa1 + (16u << 16), nbuf);
+              }
+              if (hb == 0) {
+#pragma unroll
+                for (int rho = 0; rho < 4; ++rho) {
+                  const float w = wsc[j * kBM + rq + 8 * rho];
+                  asm("mov.b64 %0, {%1, %1};" : "=l"(ws2[rho]) : "f"(w));
+                }
+              }
+              const float* ts = tsc + j * NMAX + c0 + cq + 32 * hb;
+              const float* tc = tcr + j * NMAX + c0 + cq + 32 * hb;
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const uint64_t t2 = *reinterpret_cast<const uint64_t*>(ts + 8 * v);
+                const uint64_t k2 = *reinterpret_cast<const uint64_t*>(tc + 8 * v);
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                  for (int jj = 0; jj < 2; ++jj) {
+                    const uint32_t* cur = h ? cb : ca;
+                    const int i = 4 * v + 2 * jj;
+                    promote2p(acc2[hb][2 * h + jj][v], ws2[2 * h + jj], t2, k2, cur[i], cur[i + 1]);
+                  }
+              }
+              if (u + 1 < GPS * NB32) {
+                tmem_wait_ld_pin<16>(na);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(nbuf[i]));
+              }
+            }
+          } else
 #pragma unroll
           for (int j = 0; j < GPS; ++j) {
             if (j >= gps) break;
