@@ -172,6 +172,29 @@ __device__ __forceinline__ void st_global_na_u16(uint16_t* p, uint16_t v) {
   asm volatile("st.global.L1::no_allocate.b16 [%0], %1;" ::"l"(p), "h"(v) : "memory");
 }
 
+// The 16-byte form, for whole 16-byte pieces of output rows.
+__device__ __forceinline__ void st_global_na_v4(void* p, uint4 v) {
+  asm volatile("st.global.L1::no_allocate.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// Two fp32 values -> two bf16 (round to nearest even, as float_to_bf16_bits): lo in bits 0-15, hi in 16-31.
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Four 8 x 8 b16 matrices stored transposed: thread t holds, in r[i], row t / 4 and columns 2 (t % 4),
+// 2 (t % 4) + 1 of matrix i (low half first); thread 8 i + j gives the shared address of the 16-byte row
+// j of the stored matrix i, which receives column j of the fragment.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, const uint32_t (&r)[4]) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));

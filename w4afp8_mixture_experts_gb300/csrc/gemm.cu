@@ -97,6 +97,8 @@ struct Cfg {
   static constexpr int kEpiWarps = EPIW_;   // 4 x column blocks x epilogue sets
   static constexpr int kEpiSets = EPIS_;    // epilogue sets: set c promotes groups j % EPIS == c of a stage
   static constexpr int kEpiSetWarps = EPIW_ / EPIS_;  // warps of one epilogue set (4 x column blocks)
+  static constexpr int kEpiCols = NMAX_ * 4 / (EPIW_ / EPIS_);  // columns per epilogue warp
+  static constexpr bool kEpi16 = NMAX_ >= 64 && EPIS_ == 1 && kEpiCols % 32 == 0;
   static constexpr int kWarpConv0 = kWarpMma + kMmaWarps;
   static constexpr int kWarpEpi0 = kWarpConv0 + kConvSets * kConvWarps;
   static constexpr int kWarps = kWarpEpi0 + kEpiWarps;
@@ -125,7 +127,11 @@ struct Cfg {
   static constexpr int kOffFuse = kOffSc + SSTAGES * kScBytes;
   static constexpr int kStageRow = 144;  // staged code row: 128 B + 16 B of padding (byte stores spread over banks)
   static constexpr int kFuseBytes = FUSE_ ? NMAX * kStageRow + 2 * 4 * NMAX * 4 : 0;
-  static constexpr int kOffBar = kOffFuse + kFuseBytes;
+  // 16x256b epilogues without the fused requantisation: each epilogue warp's 1 KB tile-end staging block
+  // (16 token rows x 64 B), through which stmatrix turns the weight-row-major fragments into token rows
+  static constexpr int kOffEpiStg = kOffFuse + kFuseBytes;
+  static constexpr int kEpiStgBytes = (kEpi16 && !FUSE_) ? EPIW_ * 1024 : 0;
+  static constexpr int kOffBar = kOffEpiStg + kEpiStgBytes;
   // mbarrier area, in 8-byte slots: the rings, then xfull[2], xempty[2], hx[2] (used by the fused epilogue
   // only, always laid out) and mdrain[4]; the kernel takes every array's address from these offsets
   static constexpr int kBarFull = 0, kBarEmpty = kBarFull + STAGES;
@@ -161,8 +167,6 @@ struct Cfg {
   // row per thread, makes every column's scale a 32-lane broadcast).  The fragments and the 64
   // accumulators need more registers than an even split gives, so these tiles also move registers
   // from the producer/MMA warpgroup and the converters to the epilogue warpgroups.
-  static constexpr int kEpiCols = NMAX_ * 4 / (EPIW_ / EPIS_);  // columns per epilogue warp
-  static constexpr bool kEpi16 = NMAX_ >= 64 && EPIS_ == 1 && kEpiCols % 32 == 0;
   static constexpr bool kRegSplit = kEpi16;
   // With one group per stage the MMA warps take whole stages in turn (warp m: stages st % MMAS == m)
   // instead of groups of a stage, and each stage's barriers get one commit.  A token or A slot is
@@ -198,6 +202,7 @@ struct GemmParams {
   int splits;          // K splits per tile (1: none)
   int tile_cap;        // tiles per CTA the shared-memory tile list holds (0: decode each tile in place)
   int min_rows, max_rows;  // experts with a row count outside [min_rows, max_rows] are left to another launch
+  int c_vec;               // C is 16-byte aligned: 16x256b epilogues store whole 16-byte rows of 8 columns
   // fused SiLU-and-Mul requantisation (N = 2 I): the gate tile's bf16 values go to gate [M][I] (scratch
   // read back by the same threads), the up tile's epilogue writes hq [M][I] E4M3, hs / hc [I/128][h_ld]
   uint16_t* gate;
@@ -1074,6 +1079,48 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
           }
           continue;
         }
+        if constexpr (!SPLIT && CF::kEpiStgBytes > 0) {
+          if (prm.c_vec) {
+            // The tile's bf16 values through the warp's staging block, 16 tokens at a time: an 8 x 8
+            // fragment (weight rows x tokens) is stored transposed by stmatrix, as 8 token rows of 16
+            // bytes, and read back as 16-byte pieces of token rows (8 consecutive output columns), one
+            // global store each.  Chunk c of staging row r sits at 16 * (c ^ ((r >> 1) & 3)): the 8 rows
+            // of a matrix and the 8 pieces of a quarter warp's read fall on distinct banks.
+            uint8_t* stg = smem + CF::kOffEpiStg + ew * 1024;
+            const uint32_t stg_s = smem_u32(stg);
+            const int mi = lane >> 3, mk = lane & 7;  // stmatrix row address: matrix mi (= rho), its row mk
+            const int rr = lane >> 2, rc = lane & 3;  // read-back: staging rows rr and rr + 8, chunk rc
+#pragma unroll
+            for (int hb = 0; hb < NB32; ++hb)
+#pragma unroll
+              for (int vp = 0; vp < 2; ++vp) {
+                if (c0 + 32 * hb + 16 * vp >= need) continue;  // warp-uniform: none of these 16 tokens stored
+                __syncwarp();  // the previous round's reads are done
+#pragma unroll
+                for (int vv = 0; vv < 2; ++vv) {
+                  uint32_t r[4];
+#pragma unroll
+                  for (int rho = 0; rho < 4; ++rho) {
+                    float a0, a1;
+                    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc2[hb][rho][2 * vp + vv]));
+                    r[rho] = bf16x2_bits(a0, a1);
+                  }
+                  const int row = 8 * vv + mk;  // token c0 + 32 hb + 16 vp + row
+                  stmatrix_x4_trans(stg_s + row * 64 + ((mi ^ ((row >> 1) & 3)) << 4), r);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const int row = rr + 8 * h;
+                  const int t = c0 + 32 * hb + 16 * vp + row;
+                  const uint4 w = *reinterpret_cast<const uint4*>(stg + row * 64 + ((rc ^ ((row >> 1) & 3)) << 4));
+                  if (t >= lo && t < need)
+                    st_global_na_v4(prm.C + static_cast<int64_t>(r4 + t) * prm.N + nb * kBM + q4 * 32 + 8 * rc, w);
+                }
+              }
+            continue;
+          }
+        }
 #pragma unroll
         for (int hb = 0; hb < NB32; ++hb)
 #pragma unroll
@@ -1407,6 +1454,7 @@ int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, c
   GemmParams p;
   p.seg = seg;
   p.C = C;
+  p.c_vec = reinterpret_cast<uintptr_t>(C) % 16 == 0;
   p.E = static_cast<int>(E);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
