@@ -182,6 +182,43 @@ def test_tile_configurations_agree_bit_for_bit(lib):
     assert rel_fro(f64_of_bf16(outs[0]), ref) <= 1e-3
 
 
+
+def test_output_not_16_byte_aligned(lib):
+    # 128-wide tiles store 16-byte pieces of output rows when C is 16-byte aligned; an output 2 or 6 bytes
+    # past such a boundary takes the element stores instead.  Both give the same bits, for the grouped GEMM
+    # (ragged chunks: 140 and 160 rows) and the dense Linear, and nothing outside C is written.
+    import ctypes
+    raw = lib.load()
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rng = np.random.default_rng(91)
+    M, N, K = 300, 256, 512
+    aq, a_s = _acts(rng, M, K)
+    packed, ws = _weights(rng, 2, N, K)
+    seg = np.array([0, 140, M])
+    A, S, G = to_dev(aq), scales_to_gpu_layout(a_s), scales_to_gpu_layout(gcorr_of(aq, a_s))
+    Bp, Bs, sg = prepacked(lib, packed), to_dev(ws), to_dev(seg.astype(np.int64))
+    want = lib.w4a8_grouped_gemm(A, S, G, Bp, Bs, sg)
+    assert lib.linear_split_k(M, N, K) == 1  # the Linear's tiles store C directly (no partials)
+    want_lin = lib.w4a8_linear(A, S, G, Bp[0].contiguous(), Bs[0].contiguous())
+    p = ctypes.c_void_p
+    for off in (1, 3, 8):  # 2, 6 and 16 bytes past a 256-byte aligned allocation (the last: 16-byte stores)
+        buf = torch.full((M * N + 16,), 7.0, dtype=torch.bfloat16, device="cuda")
+        C = buf[off:off + M * N]
+        assert raw.w4a8_grouped_gemm(p(A.data_ptr()), p(S.data_ptr()), p(G.data_ptr()), S.shape[1],
+                                     p(Bp.data_ptr()), p(Bs.data_ptr()), p(sg.data_ptr()), 2, N, K, M,
+                                     p(C.data_ptr()), None, 0, st) == 0
+        torch.cuda.synchronize()
+        assert torch.equal(C.view(M, N), want)
+        assert torch.all(buf[:off] == 7.0) and torch.all(buf[off + M * N:] == 7.0)
+        buf.fill_(7.0)
+        Bl, Bls = Bp[0].contiguous(), Bs[0].contiguous()
+        assert raw.w4a8_linear(p(A.data_ptr()), p(S.data_ptr()), p(G.data_ptr()), S.shape[1], p(Bl.data_ptr()),
+                               p(Bls.data_ptr()), M, N, K, p(C.data_ptr()), None, 0, st) == 0
+        torch.cuda.synchronize()
+        assert torch.equal(C.view(M, N), want_lin)
+        assert torch.all(buf[:off] == 7.0) and torch.all(buf[off + M * N:] == 7.0)
+    assert lib.device_error() == 0
+
 # The dense Linear sweep at its own shapes: M in {1, 16, 128, 1024, 8192} x (N, K) in {(24576, 1536),
 # (7168, 16384), (18432, 7168), (7168, 2048)}, with the bench's weights (counter-based generator, filled
 # on the device) and x ~ N(0,1) quantised by the library.  Every row up to M = 128 and a seeded sample of
