@@ -183,10 +183,11 @@ def test_tile_configurations_agree_bit_for_bit(lib):
 
 
 
-def test_output_not_16_byte_aligned(lib):
-    # 128-wide tiles store 16-byte pieces of output rows when C is 16-byte aligned; an output 2 or 6 bytes
-    # past such a boundary takes the element stores instead.  Both give the same bits, for the grouped GEMM
-    # (ragged chunks: 140 and 160 rows) and the dense Linear, and nothing outside C is written.
+def test_output_alignment_and_guard_band(lib):
+    # The 128-wide tiles store 16-byte pieces of output rows, so the entry points take C only 16-byte
+    # aligned: an output 2 or 6 bytes past such a boundary is refused (invalid argument) with nothing
+    # written, and one 16 bytes past it gives the bits of a fresh allocation with nothing written outside
+    # C, for the grouped GEMM (ragged chunks: 140 and 160 rows) and the dense Linear.
     import ctypes
     raw = lib.load()
     st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
@@ -197,26 +198,34 @@ def test_output_not_16_byte_aligned(lib):
     seg = np.array([0, 140, M])
     A, S, G = to_dev(aq), scales_to_gpu_layout(a_s), scales_to_gpu_layout(gcorr_of(aq, a_s))
     Bp, Bs, sg = prepacked(lib, packed), to_dev(ws), to_dev(seg.astype(np.int64))
-    want = lib.w4a8_grouped_gemm(A, S, G, Bp, Bs, sg)
+    Bl, Bls = Bp[0].contiguous(), Bs[0].contiguous()
     assert lib.linear_split_k(M, N, K) == 1  # the Linear's tiles store C directly (no partials)
-    want_lin = lib.w4a8_linear(A, S, G, Bp[0].contiguous(), Bs[0].contiguous())
+    want = lib.w4a8_grouped_gemm(A, S, G, Bp, Bs, sg)
+    want_lin = lib.w4a8_linear(A, S, G, Bl, Bls)
     p = ctypes.c_void_p
-    for off in (1, 3, 8):  # 2, 6 and 16 bytes past a 256-byte aligned allocation (the last: 16-byte stores)
-        buf = torch.full((M * N + 16,), 7.0, dtype=torch.bfloat16, device="cuda")
-        C = buf[off:off + M * N]
-        assert raw.w4a8_grouped_gemm(p(A.data_ptr()), p(S.data_ptr()), p(G.data_ptr()), S.shape[1],
+
+    def grouped(C):
+        return raw.w4a8_grouped_gemm(p(A.data_ptr()), p(S.data_ptr()), p(G.data_ptr()), S.shape[1],
                                      p(Bp.data_ptr()), p(Bs.data_ptr()), p(sg.data_ptr()), 2, N, K, M,
-                                     p(C.data_ptr()), None, 0, st) == 0
-        torch.cuda.synchronize()
-        assert torch.equal(C.view(M, N), want)
-        assert torch.all(buf[:off] == 7.0) and torch.all(buf[off + M * N:] == 7.0)
-        buf.fill_(7.0)
-        Bl, Bls = Bp[0].contiguous(), Bs[0].contiguous()
-        assert raw.w4a8_linear(p(A.data_ptr()), p(S.data_ptr()), p(G.data_ptr()), S.shape[1], p(Bl.data_ptr()),
-                               p(Bls.data_ptr()), M, N, K, p(C.data_ptr()), None, 0, st) == 0
-        torch.cuda.synchronize()
-        assert torch.equal(C.view(M, N), want_lin)
-        assert torch.all(buf[:off] == 7.0) and torch.all(buf[off + M * N:] == 7.0)
+                                     p(C.data_ptr()), None, 0, st)
+
+    def linear(C):
+        return raw.w4a8_linear(p(A.data_ptr()), p(S.data_ptr()), p(G.data_ptr()), S.shape[1], p(Bl.data_ptr()),
+                               p(Bls.data_ptr()), M, N, K, p(C.data_ptr()), None, 0, st)
+
+    for off in (1, 3, 8):  # 2, 6 and 16 bytes past a 256-byte aligned allocation
+        for call, ref in ((grouped, want), (linear, want_lin)):
+            buf = torch.full((M * N + 16,), 7.0, dtype=torch.bfloat16, device="cuda")
+            C = buf[off:off + M * N]
+            rc = call(C)
+            torch.cuda.synchronize()
+            if off == 8:
+                assert rc == 0
+                assert torch.equal(C.view(M, N), ref)
+                assert torch.all(buf[:off] == 7.0) and torch.all(buf[off + M * N:] == 7.0)
+            else:
+                assert rc == 1  # W4A8_ERR_INVALID_ARG
+                assert torch.all(buf == 7.0)
     assert lib.device_error() == 0
 
 # The dense Linear sweep at its own shapes: M in {1, 16, 128, 1024, 8192} x (N, K) in {(24576, 1536),

@@ -202,7 +202,6 @@ struct GemmParams {
   int splits;          // K splits per tile (1: none)
   int tile_cap;        // tiles per CTA the shared-memory tile list holds (0: decode each tile in place)
   int min_rows, max_rows;  // experts with a row count outside [min_rows, max_rows] are left to another launch
-  int c_vec;               // C is 16-byte aligned: 16x256b epilogues store whole 16-byte rows of 8 columns
   // fused SiLU-and-Mul requantisation (N = 2 I): the gate tile's bf16 values go to gate [M][I] (scratch
   // read back by the same threads), the up tile's epilogue writes hq [M][I] E4M3, hs / hc [I/128][h_ld]
   uint16_t* gate;
@@ -1080,46 +1079,45 @@ __global__ void __launch_bounds__(CF::kThreads, 1)
           continue;
         }
         if constexpr (!SPLIT && CF::kEpiStgBytes > 0) {
-          if (prm.c_vec) {
-            // The tile's bf16 values through the warp's staging block, 16 tokens at a time: an 8 x 8
-            // fragment (weight rows x tokens) is stored transposed by stmatrix, as 8 token rows of 16
-            // bytes, and read back as 16-byte pieces of token rows (8 consecutive output columns), one
-            // global store each.  Chunk c of staging row r sits at 16 * (c ^ ((r >> 1) & 3)): the 8 rows
-            // of a matrix and the 8 pieces of a quarter warp's read fall on distinct banks.
-            uint8_t* stg = smem + CF::kOffEpiStg + ew * 1024;
-            const uint32_t stg_s = smem_u32(stg);
-            const int mi = lane >> 3, mk = lane & 7;  // stmatrix row address: matrix mi (= rho), its row mk
-            const int rr = lane >> 2, rc = lane & 3;  // read-back: staging rows rr and rr + 8, chunk rc
+          // The tile's bf16 values through the warp's staging block, 16 tokens at a time: an 8 x 8
+          // fragment (weight rows x tokens) is stored transposed by stmatrix, as 8 token rows of 16
+          // bytes, and read back as 16-byte pieces of token rows (8 consecutive output columns), one
+          // global store each (C is 16-byte aligned, as the entry points require, and N a multiple of
+          // 128).  Chunk c of staging row r sits at 16 * (c ^ ((r >> 1) & 3)): the 8 rows of a matrix
+          // and the 8 pieces of a quarter warp's read fall on distinct banks.
+          uint8_t* stg = smem + CF::kOffEpiStg + ew * 1024;
+          const uint32_t stg_s = smem_u32(stg);
+          const int mi = lane >> 3, mk = lane & 7;  // stmatrix row address: matrix mi (= rho), its row mk
+          const int rr = lane >> 2, rc = lane & 3;  // read-back: staging rows rr and rr + 8, chunk rc
 #pragma unroll
-            for (int hb = 0; hb < NB32; ++hb)
+          for (int hb = 0; hb < NB32; ++hb)
 #pragma unroll
-              for (int vp = 0; vp < 2; ++vp) {
-                if (c0 + 32 * hb + 16 * vp >= need) continue;  // warp-uniform: none of these 16 tokens stored
-                __syncwarp();  // the previous round's reads are done
+            for (int vp = 0; vp < 2; ++vp) {
+              if (c0 + 32 * hb + 16 * vp >= need) continue;  // warp-uniform: none of these 16 tokens stored
+              __syncwarp();  // the previous round's reads are done
 #pragma unroll
-                for (int vv = 0; vv < 2; ++vv) {
-                  uint32_t r[4];
+              for (int vv = 0; vv < 2; ++vv) {
+                uint32_t r[4];
 #pragma unroll
-                  for (int rho = 0; rho < 4; ++rho) {
-                    float a0, a1;
-                    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc2[hb][rho][2 * vp + vv]));
-                    r[rho] = bf16x2_bits(a0, a1);
-                  }
-                  const int row = 8 * vv + mk;  // token c0 + 32 hb + 16 vp + row
-                  stmatrix_x4_trans(stg_s + row * 64 + ((mi ^ ((row >> 1) & 3)) << 4), r);
+                for (int rho = 0; rho < 4; ++rho) {
+                  float a0, a1;
+                  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc2[hb][rho][2 * vp + vv]));
+                  r[rho] = bf16x2_bits(a0, a1);
                 }
-                __syncwarp();
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  const int row = rr + 8 * h;
-                  const int t = c0 + 32 * hb + 16 * vp + row;
-                  const uint4 w = *reinterpret_cast<const uint4*>(stg + row * 64 + ((rc ^ ((row >> 1) & 3)) << 4));
-                  if (t >= lo && t < need)
-                    st_global_na_v4(prm.C + static_cast<int64_t>(r4 + t) * prm.N + nb * kBM + q4 * 32 + 8 * rc, w);
-                }
+                const int row = 8 * vv + mk;  // token c0 + 32 hb + 16 vp + row
+                stmatrix_x4_trans(stg_s + row * 64 + ((mi ^ ((row >> 1) & 3)) << 4), r);
               }
-            continue;
-          }
+              __syncwarp();
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int row = rr + 8 * h;
+                const int t = c0 + 32 * hb + 16 * vp + row;
+                const uint4 w = *reinterpret_cast<const uint4*>(stg + row * 64 + ((rc ^ ((row >> 1) & 3)) << 4));
+                if (t >= lo && t < need)
+                  st_global_na_v4(prm.C + static_cast<int64_t>(r4 + t) * prm.N + nb * kBM + q4 * 32 + 8 * rc, w);
+              }
+            }
+          continue;
         }
 #pragma unroll
         for (int hb = 0; hb < NB32; ++hb)
@@ -1454,7 +1452,6 @@ int launch(const uint8_t* A, const float* a_s, const float* a_c, int64_t a_ld, c
   GemmParams p;
   p.seg = seg;
   p.C = C;
-  p.c_vec = reinterpret_cast<uintptr_t>(C) % 16 == 0;
   p.E = static_cast<int>(E);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
